@@ -1,0 +1,401 @@
+"""Benchmark of the FP32 GEMM C ABI on GB300: one JSON line per run.
+
+A step is one call of the C-ABI ``sgemm`` (the whole hot path: variant
+selection, the TMA/FFMA tile kernel and, where the schedule splits tiles, the
+in-kernel Stream-K fix-up) on the square 4096 x 4096 x 4096 FP32 problem
+with i.i.d. uniform[-1, 1] inputs, already resident in HBM.  L2 is flushed
+before every timed step by writing a buffer twice the L2 size, and every step
+is timed with CUDA events on the launching stream (the flush is outside the
+events), as in "Beyond Kernel 7", section "The confirmed result".
+Throughput counts 2*M*N*K operations per call (an FFMA counts as two).
+
+Also reported: the same metric end to end through the C ABI with pinned host
+buffers (host-to-device copies of A and B and the device-to-host copy of C
+inside each timed step), the 1024^3 problem as a secondary figure, the
+roofline position of the tile kernel against the FP32 FFMA peak
+(SMs x 128 FFMA/clk x 2 FLOP x clock), and the CPU oracle timed on a bounded
+row sample of the same problem on the host cores.
+
+``--impl reference`` times only the oracle (a plain float64 triple loop on the
+host cores) on the same workload and metric.  ``--gpus N`` under torchrun
+runs N independent replicas (the product does not shard across GPUs).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "FP32 SGEMM TFLOPS (and % of GB300 FFMA peak) at n=1024/4096"
+UNIT = "TFLOP/s"
+FFMA_PER_CLK_PER_SM = 128  # FP32 lanes per SM: one FFMA each per clock
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="square_4096_uniform")
+    p.add_argument("--variant", default="auto")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="target host time of the oracle sample")
+    p.add_argument("--sweep", action="store_true",
+                   help="one JSON line per workload of the configuration list (not the default line)")
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------ distribution
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest value of ``x`` over all ranks (timing: the slowest replica decides)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(per_rank_flops: float, max_seconds: float, world: int) -> float:
+    """Whole-job throughput: the work of all replicas over the slowest replica's time."""
+    return per_rank_flops * world / max_seconds / 1e12
+
+
+# ------------------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples SM clock and throttle reasons with nvidia-smi while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power)}
+
+
+# -------------------------------------------------------------------- GPU timing
+def time_steps(fn, steps, warmup, flush=None, stream=None):
+    """Per-step device times (ms) of ``fn`` with CUDA events on ``stream``; ``flush`` runs
+    before each step outside the events."""
+    import torch
+    stream = stream or torch.cuda.current_stream()
+    for _ in range(warmup):
+        if flush:
+            flush()
+        fn()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        if flush:
+            flush()
+        starts[i].record(stream)
+        fn()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def ffma_peak_tflops(sms: int, mhz: float) -> float:
+    return sms * FFMA_PER_CLK_PER_SM * 2 * mhz * 1e6 / 1e12
+
+
+def measured_traffic():
+    """DRAM bytes per launch of the tile kernel at 4096^3, from the committed ncu summary."""
+    path = os.path.join(ROOT, "profiles", "tile_kernel_4096.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("dram_bytes_per_launch"), d.get("kernel_build")
+    except (OSError, ValueError):
+        return None, None
+
+
+def cpu_baseline(w, A, B, seconds: float):
+    """Time the oracle (as it stands) on a bounded row sample of the workload."""
+    import oracle
+    cores = oracle.max_threads()
+    rows = max(1, min(w.M, cores))
+    t0 = time.perf_counter()
+    oracle.sgemm_f64(A[:rows], B, with_abs=False)
+    dt = time.perf_counter() - t0
+    rows2 = int(min(w.M, max(rows, rows * seconds / max(dt, 1e-6))))
+    rows2 = max(rows, (rows2 // cores) * cores) if rows2 >= cores else rows2
+    t0 = time.perf_counter()
+    oracle.sgemm_f64(A[:rows2], B, with_abs=False)
+    dt2 = time.perf_counter() - t0
+    flops = 2.0 * rows2 * w.N * w.K
+    return {"value": flops / dt2 / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"rows 0..{rows2 - 1} of the {w.M}x{w.N}x{w.K} product ({rows2}x{w.N} outputs, "
+                      f"float64 triple loop, {dt2:.1f} s)",
+            "seconds": dt2}
+
+
+# ------------------------------------------------------------------------- arms
+def run_reference(args):
+    """The oracle alone, on the host cores, on the same workload and metric."""
+    from dense_fp32_gemm_03_gb300 import workloads
+    import oracle
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = workloads.BY_NAME[args.workload]
+    A, B = workloads.operands(w)
+    cores = oracle.max_threads()
+    # Rows per step sized so that warm-up plus all steps take a few minutes at most.
+    rows = cores
+    t0 = time.perf_counter()
+    oracle.sgemm_f64(A[:rows], B, with_abs=False)
+    one = time.perf_counter() - t0
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(w.M, rows * budget / max(one, 1e-6))))
+    times = []
+    for i in range(args.warmup + args.steps):
+        r0 = (i * rows) % max(1, w.M - rows + 1)
+        t0 = time.perf_counter()
+        oracle.sgemm_f64(A[r0:r0 + rows], B, with_abs=False)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    per_step = sum(times) / len(times)
+    value = 2.0 * rows * w.N * w.K / per_step / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded uniform[-1,1])",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+                   "step": f"{rows} rows of C ({rows}x{w.N} outputs) per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{rows} rows of the {w.M}x{w.N}x{w.K} product per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def bench_workload(w, args, sg, device, flush, variant):
+    import torch
+    from dense_fp32_gemm_03_gb300 import workloads
+    A_h, B_h = workloads.operands(w)
+    A = A_h.to(device)
+    B = B_h.to(device)
+    C = torch.empty((w.M, w.N), device=device)
+    stream = torch.cuda.current_stream(device)
+    lda, ldb, ldc = w.K, w.N, w.N
+
+    def step():
+        st = sg.sgemm_raw(w.M, w.N, w.K, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(), ldc,
+                          stream.cuda_stream, variant)
+        if st != 0:
+            raise RuntimeError(f"sgemm failed: {sg.status_string(st)}")
+
+    times = time_steps(step, args.steps, args.warmup, flush, stream)
+    chosen = sg.select_variant(A, B, C) if variant == sg.AUTO else variant
+    return A_h, B_h, A, B, C, times, chosen
+
+
+def run_ours(args):
+    import torch
+    import dense_fp32_gemm_03_gb300 as sg
+    from dense_fp32_gemm_03_gb300 import workloads
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
+        return 1
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    from dense_fp32_gemm_03_gb300 import _build
+    _build.build()
+    sg.load()
+    variant = sg.AUTO if args.variant == "auto" else sg.VARIANTS[args.variant]
+
+    props = torch.cuda.get_device_properties(device)
+    sms = props.multi_processor_count
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    flush_buf = torch.empty(2 * l2 // 4, dtype=torch.float32, device=device)
+
+    def flush():
+        flush_buf.fill_(1.0)
+
+    if args.sweep:
+        for w in workloads.ALL:
+            if w.dist == "int8range":
+                continue
+            *_, times, chosen = bench_workload(w, args, sg, device, flush, variant)
+            ms = statistics.median(times)
+            print(json.dumps({"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+                              "variant": sg.variant_name(chosen), "us_median": ms * 1e3,
+                              "us_p10": sorted(times)[len(times) // 10] * 1e3,
+                              "us_p90": sorted(times)[(9 * len(times)) // 10] * 1e3,
+                              "tflops": w.flops / (ms * 1e-3) / 1e12}), flush=True)
+        return 0
+
+    w = workloads.BY_NAME[args.workload]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        A_h, B_h, A, B, C, times, chosen = bench_workload(w, args, sg, device, flush, variant)
+    barrier(world)
+    torch.cuda.synchronize()
+    total_s = sum(times) / 1e3
+    max_total = max_over_ranks(total_s, world, device)
+    mean_ms = max_total / args.steps * 1e3
+    value = aggregate(w.flops * args.steps, max_total, world)
+    clock = clocks.summary()
+
+    # Roofline of the tile kernel: one launch per step, so the event time is its duration.
+    kernel_tflops = w.flops / (statistics.mean(times) * 1e-3) / 1e12
+    peak_max = ffma_peak_tflops(sms, clock["sm_max_mhz"] or 2070.0)
+    peak_run = ffma_peak_tflops(sms, clock["sm_mhz"]) if clock["sm_mhz"] else None
+    traffic, _ = measured_traffic()
+
+    # End to end through the C ABI with pinned host buffers.
+    A_pin = A_h.pin_memory()
+    B_pin = B_h.pin_memory()
+    C_pin = torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream(device)
+
+    def e2e_step():
+        A.copy_(A_pin, non_blocking=True)
+        B.copy_(B_pin, non_blocking=True)
+        st = sg.sgemm_raw(w.M, w.N, w.K, A.data_ptr(), w.K, B.data_ptr(), w.N, C.data_ptr(), w.N,
+                          stream.cuda_stream, variant)
+        if st != 0:
+            raise RuntimeError(sg.status_string(st))
+        C_pin.copy_(C, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    e2e_times = time_steps(e2e_step, e2e_steps, 2, flush, stream)
+    e2e_total = max_over_ranks(sum(e2e_times) / 1e3, world, device)
+    e2e_value = aggregate(w.flops * e2e_steps, e2e_total, world)
+
+    # Secondary size (n = 1024) on the same device.
+    w2 = workloads.SQUARE_1024
+    *_, times2, chosen2 = bench_workload(w2, args, sg, device, flush, variant)
+    t2 = max_over_ranks(sum(times2) / 1e3, world, device)
+    value2 = aggregate(w2.flops * args.steps, t2, world)
+
+    status, site = sg.query_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} at wait site {site}")
+
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded uniform[-1,1], generated on the host)",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": "row-major",
+                   "variant": sg.variant_name(chosen), "l2": "flushed before each step (2x L2 write)",
+                   "us_median": statistics.median(times) * 1e3,
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "pct_ffma_peak": {"at_max_clock": 100 * kernel_tflops / peak_max,
+                          "at_measured_clock": (100 * kernel_tflops / peak_run) if peak_run else None},
+        "roofline": {"bound": "alu", "achieved": kernel_tflops, "peak": peak_max, "unit": UNIT,
+                     "frac": kernel_tflops / peak_max, "traffic": traffic,
+                     "peak_basis": f"{sms} SMs x {FFMA_PER_CLK_PER_SM} FFMA/clk x 2 x "
+                                   f"{clock['sm_max_mhz'] or 2070.0:.0f} MHz (max SM clock)",
+                     "peak_at_measured_clock": peak_run},
+        "secondary": {"workload": w2.name, "value": value2, "unit": UNIT,
+                      "variant": sg.variant_name(chosen2),
+                      "us_median": statistics.median(times2) * 1e3},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 4 * (w.M * w.K + w.K * w.N),
+                "d2h_bytes_per_step": 4 * w.M * w.N},
+        "gpu_launches": args.steps,
+        "clocks": {"sm_mhz": clock["sm_mhz"], "sm_max_mhz": clock["sm_max_mhz"],
+                   "reasons": clock["reasons"], "samples": clock["samples"]},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = {k: v for k, v in cpu_baseline(w, A_h, B_h, args.cpu_seconds).items()
+                                if k != "seconds"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,423 @@
+// sgemm_api.cu -- host side of the C ABI declared in include/sgemm.h:
+// argument validation, the shape-keyed variant selector, the work
+// decomposition (whole-tile waves and Stream-K), the TMA descriptor for B,
+// the per-(device, stream) workspace cache and the device status word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "sgemm.h"
+#include "sgemm_internal.h"
+
+namespace {
+
+using gb300::Sched;
+using gb300::TileConfig;
+using gb300::TileShape;
+
+// [0] = first sgemm_status_t recorded by a kernel since the last query, [1] = wait site.
+__device__ uint32_t g_status_word[2];
+
+constexpr int64_t kInt32Max = 0x7fffffffLL;
+constexpr uint64_t kDefaultWaitLimitNs = 4000000000ull;  // 4 s: far above any legitimate wait
+constexpr int kGroupM = 8;
+constexpr int kMinSkIters = 4;  // Stream-K shares shorter than this many k-tiles are not worth splitting
+// Every workspace starts with a counter region of fixed size, so that a cached
+// workspace reused with another layout never finds partial sums where its
+// counters are: counters are zero at allocation and every call leaves them zero.
+constexpr size_t kCounterBytes = 16384;
+constexpr int64_t kMaxSplitTiles = kCounterBytes / 4;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceState {
+  sgemm_status_t init_status = SGEMM_OK;
+  int sms = 0;
+  int ctas_per_sm[gb300::kTileConfigs] = {0, 0};
+  uint32_t* status = nullptr;
+};
+
+struct Workspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceState> g_devices;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;
+EncodeTiledFn g_encode = nullptr;
+
+// Initialises (once) and returns the state of the current device.
+sgemm_status_t device_state(DeviceState** out, int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  auto it = g_devices.find(dev);
+  if (it == g_devices.end()) {
+    DeviceState st;
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3) {
+      st.init_status = SGEMM_ERR_UNSUPPORTED;  // the library carries sm_103a code only
+    } else {
+      cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev);
+      for (int c = 0; c < gb300::kTileConfigs; ++c) {
+        st.ctas_per_sm[c] = gb300::tile_kernel_prepare(TileConfig(c));
+        if (st.ctas_per_sm[c] <= 0) st.init_status = SGEMM_ERR_LAUNCH;
+      }
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) {
+        st.init_status = SGEMM_ERR_LAUNCH;
+      } else {
+        st.status = static_cast<uint32_t*>(p);
+        if (cudaMemset(p, 0, sizeof(g_status_word)) != cudaSuccess) st.init_status = SGEMM_ERR_LAUNCH;
+      }
+      if (g_encode == nullptr) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess) {
+          g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        } else {
+          st.init_status = SGEMM_ERR_UNSUPPORTED;
+        }
+      }
+    }
+    cudaGetLastError();  // attribute queries must not leak a sticky error into the caller
+    it = g_devices.emplace(dev, st).first;
+  }
+  *out = &it->second;
+  if (dev_out) *dev_out = dev;
+  return it->second.init_status;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const float* a, int64_t rows, int64_t cols, int64_t ld, const float* c,
+              int64_t crows, int64_t ccols, int64_t ldc) {
+  if (rows == 0 || cols == 0 || crows == 0 || ccols == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a);
+  const uintptr_t a1 = a0 + uintptr_t(((rows - 1) * ld + cols) * 4);
+  const uintptr_t c0 = reinterpret_cast<uintptr_t>(c);
+  const uintptr_t c1 = c0 + uintptr_t(((crows - 1) * ldc + ccols) * 4);
+  return a0 < c1 && c0 < a1;
+}
+
+sgemm_status_t validate(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+                        const float* B, int64_t ldb, const float* C, int64_t ldc) {
+  if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_VALUE;
+  if (M > kInt32Max || N > kInt32Max || K > kInt32Max) return SGEMM_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return SGEMM_OK;
+  if (C == nullptr || ldc < N) return SGEMM_ERR_INVALID_VALUE;
+  if (K == 0) return SGEMM_OK;
+  if (A == nullptr || B == nullptr || lda < K || ldb < N) return SGEMM_ERR_INVALID_VALUE;
+  if (overlaps(A, M, K, lda, C, M, N, ldc) || overlaps(B, K, N, ldb, C, M, N, ldc))
+    return SGEMM_ERR_INVALID_VALUE;
+  return SGEMM_OK;
+}
+
+bool fast_path_ok(const float* A, int64_t lda, const float* B, int64_t ldb, const float* C,
+                  int64_t ldc) {
+  return aligned16(A) && aligned16(B) && aligned16(C) && lda % 4 == 0 && ldb % 4 == 0 &&
+         ldc % 4 == 0;
+}
+
+struct Plan {
+  int variant = -1;
+  TileConfig cfg = gb300::kTileLarge;
+  Sched sc{};
+  int grid = 0;
+  size_t partial_bytes = 0;
+  size_t workspace_bytes() const { return partial_bytes ? kCounterBytes + partial_bytes : 0; }
+};
+
+bool is_fast(int v) {
+  return v == SGEMM_VARIANT_TILED || v == SGEMM_VARIANT_STREAMK ||
+         v == SGEMM_VARIANT_TILED_SMALL || v == SGEMM_VARIANT_STREAMK_SMALL;
+}
+
+// Work decomposition of a fast variant.
+bool make_plan(int variant, int64_t M, int64_t N, int64_t K, const DeviceState& ds, Plan* p) {
+  p->variant = variant;
+  if (!is_fast(variant)) return true;
+  p->cfg = (variant == SGEMM_VARIANT_TILED_SMALL || variant == SGEMM_VARIANT_STREAMK_SMALL)
+               ? gb300::kTileSmall
+               : gb300::kTileLarge;
+  const TileShape ts = gb300::tile_shape(p->cfg);
+  const int64_t tiles_m = (M + ts.bm - 1) / ts.bm, tiles_n = (N + ts.bn - 1) / ts.bn;
+  const int64_t tiles = tiles_m * tiles_n;
+  const int64_t ipt = (K + ts.bk - 1) / ts.bk;
+  if (tiles > kInt32Max || ipt > kInt32Max) return false;
+  Sched& sc = p->sc;
+  sc.tiles_m = int(tiles_m);
+  sc.tiles_n = int(tiles_n);
+  sc.group_m = kGroupM;
+  sc.iters_per_tile = int(ipt);
+  const bool streamk = (variant == SGEMM_VARIANT_STREAMK || variant == SGEMM_VARIANT_STREAMK_SMALL);
+  const int64_t resident = int64_t(ds.sms) * ds.ctas_per_sm[p->cfg];
+  if (!streamk || resident <= 0) {
+    sc.dp_tiles = int(tiles);
+    p->grid = int(tiles);
+    return true;
+  }
+  // Persistent: as many CTAs as fit at once.  Whole tiles fill complete
+  // waves; the tiles of the last, partial wave are shared out over K.
+  const int64_t waves = tiles / resident;
+  const int64_t rem = tiles % resident;
+  sc.dp_tiles = int(waves * resident);
+  sc.sk_tiles = int(rem);
+  p->grid = int(tiles < resident ? tiles : resident);
+  if (rem > 0) {
+    const int64_t total = rem * ipt;
+    int64_t sk_ctas = resident;
+    if (total / sk_ctas < kMinSkIters) sk_ctas = total / kMinSkIters;
+    if (sk_ctas < rem) sk_ctas = rem;  // never fewer sharers than tiles
+    if (sk_ctas > resident) sk_ctas = resident;
+    sc.sk_ctas = int(sk_ctas);
+    sc.sk_base = int(total / sk_ctas);
+    sc.sk_extra = int(total % sk_ctas);
+    p->grid = int(sc.dp_tiles > 0 ? resident : sk_ctas);
+    if (rem > kMaxSplitTiles) return false;
+    const int64_t slots = rem + sk_ctas - 1;
+    p->partial_bytes = size_t(slots) * ts.bm * ts.bn * 4;
+  }
+  return true;
+}
+
+// The selector: aligned operands take a pipelined variant, the rest the guarded kernel.
+int select_variant(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
+                   int64_t ldb, const float* C, int64_t ldc, const DeviceState& ds) {
+  if (!fast_path_ok(A, lda, B, ldb, C, ldc)) return SGEMM_VARIANT_GUARDED;
+  // Estimated time of each candidate in units of one large-tile k-iteration on
+  // one SM: the busiest SM's share of the k-tiles, plus a charge per split.
+  int best = SGEMM_VARIANT_STREAMK;
+  double best_cost = 1e300;
+  const int candidates[4] = {SGEMM_VARIANT_STREAMK, SGEMM_VARIANT_TILED,
+                             SGEMM_VARIANT_STREAMK_SMALL, SGEMM_VARIANT_TILED_SMALL};
+  for (int v : candidates) {
+    Plan p;
+    if (!make_plan(v, M, N, K, ds, &p)) continue;
+    const TileShape ts = gb300::tile_shape(p.cfg);
+    const double tile_work = double(ts.bm) * ts.bn / (128.0 * 256.0);  // relative to a large tile
+    const int cps = ds.ctas_per_sm[p.cfg];
+    const double ipt = p.sc.iters_per_tile;
+    double cost;
+    if (p.sc.sk_tiles == 0) {
+      const int64_t resident = int64_t(ds.sms) * cps;
+      const int64_t tiles = int64_t(p.sc.tiles_m) * p.sc.tiles_n;
+      const int64_t waves = (tiles + resident - 1) / resident;
+      cost = double(waves) * ipt * tile_work * cps;
+    } else {
+      const double per_cta = double(p.sc.sk_base + (p.sc.sk_extra ? 1 : 0));
+      const double dp_waves = p.sc.dp_tiles / double(int64_t(ds.sms) * cps);
+      cost = (dp_waves * ipt + per_cta) * tile_work * cps + 2.0 * tile_work;  // fixup ~ 2 k-tiles
+    }
+    if (cost < best_cost * 0.999) {
+      best_cost = cost;
+      best = v;
+    }
+  }
+  return best;
+}
+
+sgemm_status_t get_workspace(int dev, cudaStream_t stream, const Plan& p, void** out) {
+  const size_t need = p.workspace_bytes();
+  *out = nullptr;
+  if (need == 0) return SGEMM_OK;
+  std::lock_guard<std::mutex> lock(g_mu);
+  Workspace& ws = g_workspaces[{dev, stream}];
+  if (ws.bytes < need) {
+    if (ws.ptr) {
+      cudaFree(ws.ptr);  // cudaFree waits for the device, so no kernel still uses it
+      ws.ptr = nullptr;
+      ws.bytes = 0;
+    }
+    size_t bytes = need + need / 4;
+    if (cudaMalloc(&ws.ptr, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      return SGEMM_ERR_ALLOC;
+    }
+    // Arrival counters start at zero; every finished tile resets its own.
+    if (cudaMemsetAsync(ws.ptr, 0, bytes, stream) != cudaSuccess) {
+      cudaFree(ws.ptr);
+      ws.ptr = nullptr;
+      return SGEMM_ERR_LAUNCH;
+    }
+    ws.bytes = bytes;
+  }
+  *out = ws.ptr;
+  return SGEMM_OK;
+}
+
+sgemm_status_t run(int variant, int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+                   const float* B, int64_t ldb, float* C, int64_t ldc, cudaStream_t stream) {
+  sgemm_status_t st = validate(M, N, K, A, lda, B, ldb, C, ldc);
+  if (st != SGEMM_OK) return st;
+  if (variant < SGEMM_VARIANT_AUTO || variant >= SGEMM_VARIANT_COUNT) return SGEMM_ERR_INVALID_VALUE;
+  DeviceState* ds = nullptr;
+  int dev = 0;
+  st = device_state(&ds, &dev);
+  if (st != SGEMM_OK) return st;
+  if (M == 0 || N == 0) return SGEMM_OK;
+  if (K == 0) {
+    return gb300::launch_zero_fill(M, N, C, ldc, stream) == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+  }
+  if (variant == SGEMM_VARIANT_AUTO) variant = select_variant(M, N, K, A, lda, B, ldb, C, ldc, *ds);
+  if (variant == SGEMM_VARIANT_GUARDED) {
+    return gb300::launch_guarded_kernel(M, N, K, A, lda, B, ldb, C, ldc, stream) == cudaSuccess
+               ? SGEMM_OK
+               : SGEMM_ERR_LAUNCH;
+  }
+  if (!fast_path_ok(A, lda, B, ldb, C, ldc)) return SGEMM_ERR_INVALID_VALUE;
+  Plan p;
+  if (!make_plan(variant, M, N, K, *ds, &p)) return SGEMM_ERR_UNSUPPORTED;
+  const TileShape ts = gb300::tile_shape(p.cfg);
+
+  CUtensorMap tmap;
+  std::memset(&tmap, 0, sizeof(tmap));
+  const cuuint64_t dims[2] = {cuuint64_t(N), cuuint64_t(K)};
+  const cuuint64_t strides[1] = {cuuint64_t(ldb) * 4};
+  const cuuint32_t box[2] = {cuuint32_t(ts.bn), cuuint32_t(ts.bk)};
+  const cuuint32_t estr[2] = {1, 1};
+  if (g_encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(B), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return SGEMM_ERR_LAUNCH;
+
+  void* ws = nullptr;
+  st = get_workspace(dev, stream, p, &ws);
+  if (st != SGEMM_OK) return st;
+  gb300::GemmArgs args{};
+  args.M = int(M);
+  args.N = int(N);
+  args.K = int(K);
+  args.A = A;
+  args.lda = lda;
+  args.C = C;
+  args.ldc = ldc;
+  args.counters = static_cast<int32_t*>(ws);
+  args.partials = ws ? reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes) : nullptr;
+  args.status = ds->status;
+  args.wait_limit_ns = kDefaultWaitLimitNs;
+  return gb300::launch_tile_kernel(p.cfg, tmap, args, p.sc, p.grid, stream) == cudaSuccess
+             ? SGEMM_OK
+             : SGEMM_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+sgemm_status_t sgemm(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
+                     int64_t ldb, float* C, int64_t ldc, cudaStream_t stream) {
+  return run(SGEMM_VARIANT_AUTO, M, N, K, A, lda, B, ldb, C, ldc, stream);
+}
+
+sgemm_status_t sgemm_variant(int variant, int64_t M, int64_t N, int64_t K, const float* A,
+                             int64_t lda, const float* B, int64_t ldb, float* C, int64_t ldc,
+                             cudaStream_t stream) {
+  return run(variant, M, N, K, A, lda, B, ldb, C, ldc, stream);
+}
+
+int sgemm_select_variant(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+                         const float* B, int64_t ldb, const float* C, int64_t ldc) {
+  if (validate(M, N, K, A, lda, B, ldb, C, ldc) != SGEMM_OK) return -1;
+  DeviceState* ds = nullptr;
+  if (device_state(&ds, nullptr) != SGEMM_OK) return -1;
+  return select_variant(M, N, K, A, lda, B, ldb, C, ldc, *ds);
+}
+
+size_t sgemm_workspace_size(int variant, int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0 || M > kInt32Max || N > kInt32Max || K > kInt32Max) return 0;
+  DeviceState* ds = nullptr;
+  if (device_state(&ds, nullptr) != SGEMM_OK) return 0;
+  if (variant == SGEMM_VARIANT_AUTO) {
+    // Aligned operands are assumed (the guarded kernel needs no workspace).
+    const float* p = reinterpret_cast<const float*>(uintptr_t(256));
+    variant = select_variant(M, N, K, p, (K + 3) / 4 * 4, p, (N + 3) / 4 * 4, p, (N + 3) / 4 * 4, *ds);
+  }
+  Plan p;
+  if (!make_plan(variant, M, N, K, *ds, &p)) return 0;
+  return p.workspace_bytes();
+}
+
+sgemm_status_t sgemm_query_device_status(cudaStream_t stream, uint32_t* detail) {
+  DeviceState* ds = nullptr;
+  int dev = 0;
+  sgemm_status_t st = device_state(&ds, &dev);
+  if (detail) *detail = 0;
+  if (st != SGEMM_OK) return st;
+  uint32_t word[2] = {0, 0};
+  if (cudaStreamSynchronize(stream) != cudaSuccess ||
+      cudaMemcpy(word, ds->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(ds->status, 0, sizeof(word)) != cudaSuccess)
+    return SGEMM_ERR_LAUNCH;
+  if (detail) *detail = word[1];
+  if (word[0] == SGEMM_OK) return SGEMM_OK;
+  // A kernel gave up part-way: its arrival counters may be left nonzero.
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (auto& kv : g_workspaces)
+      if (kv.first.first == dev && kv.second.ptr) cudaMemset(kv.second.ptr, 0, kv.second.bytes);
+  }
+  return sgemm_status_t(word[0]);
+}
+
+void sgemm_release_workspaces(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int cur = 0;
+  cudaGetDevice(&cur);
+  for (auto& kv : g_workspaces) {
+    if (kv.second.ptr) {
+      cudaSetDevice(kv.first.first);
+      cudaDeviceSynchronize();
+      cudaFree(kv.second.ptr);
+    }
+  }
+  g_workspaces.clear();
+  cudaSetDevice(cur);
+}
+
+const char* sgemm_status_string(sgemm_status_t s) {
+  switch (s) {
+    case SGEMM_OK: return "ok";
+    case SGEMM_ERR_INVALID_VALUE: return "invalid argument";
+    case SGEMM_ERR_LAUNCH: return "CUDA launch or API call failed";
+    case SGEMM_ERR_TIMEOUT: return "device wait exceeded its time limit";
+    case SGEMM_ERR_UNSUPPORTED: return "unsupported device or size";
+    case SGEMM_ERR_ALLOC: return "workspace allocation failed";
+  }
+  return "unknown status";
+}
+
+const char* sgemm_variant_name(int v) {
+  switch (v) {
+    case SGEMM_VARIANT_GUARDED: return "guarded";
+    case SGEMM_VARIANT_TILED: return "tiled";
+    case SGEMM_VARIANT_STREAMK: return "streamk";
+    case SGEMM_VARIANT_TILED_SMALL: return "tiled_small";
+    case SGEMM_VARIANT_STREAMK_SMALL: return "streamk_small";
+  }
+  return "unknown";
+}
+
+sgemm_status_t sgemm_debug_expire_wait(uint64_t limit_ns, cudaStream_t stream) {
+  DeviceState* ds = nullptr;
+  sgemm_status_t st = device_state(&ds, nullptr);
+  if (st != SGEMM_OK) return st;
+  if (limit_ns > 10000000000ull) return SGEMM_ERR_INVALID_VALUE;  // keep the probe short
+  return gb300::launch_expire_probe(ds->status, limit_ns, stream) == cudaSuccess ? SGEMM_OK
+                                                                                 : SGEMM_ERR_LAUNCH;
+}
+
+}  // extern "C"

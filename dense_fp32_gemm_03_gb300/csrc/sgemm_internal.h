@@ -1,0 +1,77 @@
+// sgemm_internal.h -- declarations shared by the host API and the kernel translation units.
+// Not installed; the public interface is include/sgemm.h.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+
+namespace gb300 {
+
+// Codes written to the device status word (detail) when a bounded wait expires.
+enum WaitSite : uint32_t {
+  kWaitNone = 0,
+  kWaitTileStage = 1,   // a compute thread waiting for a B stage (TMA) to land
+  kWaitDrain = 2,       // draining in-flight copies after an error
+  kWaitDebugProbe = 3,  // the deliberate expiry hook
+};
+
+// Work decomposition of one launch of the tile kernel (host-computed).
+//
+// The output is cut into tiles_m x tiles_n tiles of BM x BN, visited in a
+// grouped ("swizzled") order of `group_m` tile rows.  Tiles [0, dp_tiles) are
+// computed whole, tile c + w * gridDim.x by CTA c.  The K iterations of tiles
+// [dp_tiles, dp_tiles + sk_tiles) form one stream that is cut evenly over the
+// first sk_ctas CTAs (Stream-K): CTA c < sk_ctas owns iterations
+// [c * sk_base + min(c, sk_extra), ...) of length sk_base + (c < sk_extra).  A tile whose K range is shared by
+// several CTAs is finished by whichever of them arrives last, which adds the
+// partial sums in CTA order (deterministic).
+struct Sched {
+  int32_t tiles_m, tiles_n;
+  int32_t group_m;
+  int32_t iters_per_tile;  // ceil(K / BK)
+  int32_t dp_tiles;
+  int32_t sk_tiles;
+  int32_t sk_ctas;
+  int32_t sk_base, sk_extra;
+};
+
+struct GemmArgs {
+  int32_t M, N, K;
+  const float* A;
+  int64_t lda;
+  float* C;
+  int64_t ldc;
+  float* partials;      // Stream-K partial tiles (sk_tiles + gridDim.x - 1 slots), or null
+  int32_t* counters;    // one arrival counter per split tile, zero on entry, zero on exit
+  uint32_t* status;     // device status word: [0] = sgemm_status_t, [1] = WaitSite
+  uint64_t wait_limit_ns;
+};
+
+// Tile configurations of the pipelined kernel.
+enum TileConfig : int { kTileLarge = 0, kTileSmall = 1, kTileConfigs = 2 };
+
+struct TileShape {
+  int bm, bn, bk, threads, stages;
+  size_t smem_bytes;
+};
+
+TileShape tile_shape(TileConfig cfg);
+
+// Sets the kernel attributes (dynamic shared memory) once per device and
+// returns the resident CTAs per SM, or a negative value on error.
+int tile_kernel_prepare(TileConfig cfg);
+
+cudaError_t launch_tile_kernel(TileConfig cfg, const CUtensorMap& tmap_b, const GemmArgs& args,
+                               const Sched& sched, int grid, cudaStream_t stream);
+
+cudaError_t launch_guarded_kernel(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+                                  const float* B, int64_t ldb, float* C, int64_t ldc,
+                                  cudaStream_t stream);
+
+cudaError_t launch_zero_fill(int64_t M, int64_t N, float* C, int64_t ldc, cudaStream_t stream);
+
+cudaError_t launch_expire_probe(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace gb300

@@ -1,0 +1,128 @@
+/*
+ * sgemm.h -- C ABI of the GB300 (sm_103a) single-precision GEMM library.
+ *
+ * Operation.  C = A * B for row-major FP32 matrices, A (M x K), B (K x N),
+ * C (M x N):  C[m, n] = sum over k of A[m, k] * B[k, n], accumulated with
+ * FP32 fused multiply-adds (no TF32, no reduced-precision tensor path).
+ * Definition: "Beyond Kernel 7: Closing the Gap to cuBLAS on an H100 FP32
+ * GEMM", section "The operation: GEMM and the precision of the comparison"
+ * (C[m, n] = sum_k A[m, k] B[k, n]; only A*B is computed, i.e. alpha = 1 and
+ * beta = 0; about 2MNK operations, an FFMA counting as two).  Row-major
+ * storage follows the same page's "Kernel 1" section; element (r, c) of a
+ * matrix with row stride ld sits at base[r * ld + c].
+ *
+ * Memory and ownership.  A, B and C are DEVICE pointers owned by the caller;
+ * the library never frees or retains them past the call.  C must not overlap
+ * A or B.  C is write-only: its previous contents (NaN included) are never
+ * read.  All calls are asynchronous on `stream` (0 = legacy default stream):
+ * they return once the kernels are enqueued.
+ *
+ * Scratch.  Shapes that the split-K (Stream-K) schedule serves use a device
+ * workspace.  sgemm()/sgemm_variant() take it from a cache the library keeps
+ * per (device, stream): the first call that needs more than the cache holds
+ * allocates it with cudaMalloc (so make that first call outside stream
+ * capture); later calls reuse it.  Calls on one stream are ordered; calls on
+ * different streams use different workspaces.  sgemm_release_workspaces()
+ * frees the cache.
+ *
+ * Errors.  Every entry point returns an sgemm_status_t and never aborts the
+ * process.  Argument errors are found on the host before any launch.  A
+ * device-side wait that exceeds its time limit (a pipeline that stopped
+ * making progress) makes the kernel record SGEMM_ERR_TIMEOUT in a device
+ * status word and return early instead of hanging; read it with
+ * sgemm_query_device_status().
+ */
+#ifndef GB300_SGEMM_H
+#define GB300_SGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SGEMM_OK = 0,
+  SGEMM_ERR_INVALID_VALUE = 1, /* negative size, ld too small, NULL with nonzero extent, bad variant */
+  SGEMM_ERR_LAUNCH = 2,        /* a CUDA launch or API call failed (see cudaGetLastError) */
+  SGEMM_ERR_TIMEOUT = 3,       /* a kernel's bounded wait expired; its output is not valid */
+  SGEMM_ERR_UNSUPPORTED = 4,   /* no sm_103a device, or a size beyond 2^31 - 1 */
+  SGEMM_ERR_ALLOC = 5          /* the workspace cache could not be allocated */
+} sgemm_status_t;
+
+/* Kernel variants, for sgemm_variant() and sgemm_select_variant(). */
+typedef enum {
+  SGEMM_VARIANT_AUTO = -1,     /* let the selector choose (what sgemm() does) */
+  SGEMM_VARIANT_GUARDED = 0,   /* any shape, stride and alignment; bounds-checked scalar loads */
+  SGEMM_VARIANT_TILED = 1,     /* pipelined 128x256 tiles, one output tile per CTA, no split */
+  SGEMM_VARIANT_STREAMK = 2,   /* persistent CTAs: whole tiles in full waves, the rest split over K */
+  SGEMM_VARIANT_TILED_SMALL = 3,   /* pipelined 128x128 tiles, one output tile per CTA */
+  SGEMM_VARIANT_STREAMK_SMALL = 4, /* Stream-K schedule over 128x128 tiles */
+  SGEMM_VARIANT_COUNT = 5
+} sgemm_variant_t;
+
+/*
+ * C = A * B.  M, N, K >= 0; lda >= K, ldb >= N, ldc >= N (elements).
+ * M == 0 or N == 0: nothing to do, SGEMM_OK.  K == 0: C is filled with zeros
+ * (the empty sum).  Any stride and alignment is accepted; the fast kernels
+ * need 16-byte-aligned A, B, C and lda, ldb, ldc multiples of 4, and other
+ * inputs take the bounds-checked kernel.
+ */
+sgemm_status_t sgemm(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                     const float *B, int64_t ldb, float *C, int64_t ldc, cudaStream_t stream);
+
+/*
+ * As sgemm() but forces `variant` (an sgemm_variant_t).  A fast variant given
+ * operands it cannot take (misaligned pointer or stride) returns
+ * SGEMM_ERR_INVALID_VALUE without launching.
+ */
+sgemm_status_t sgemm_variant(int variant, int64_t M, int64_t N, int64_t K, const float *A,
+                             int64_t lda, const float *B, int64_t ldb, float *C, int64_t ldc,
+                             cudaStream_t stream);
+
+/*
+ * The variant sgemm() would run for these arguments on the current device
+ * (pointers are used only for their alignment), or -1 if the arguments are
+ * invalid.  Launches nothing.
+ */
+int sgemm_select_variant(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                         const float *B, int64_t ldb, const float *C, int64_t ldc);
+
+/*
+ * Bytes of workspace the given variant (or the selected one, for
+ * SGEMM_VARIANT_AUTO) needs for this shape on the current device; 0 when it
+ * needs none.  Returns 0 for invalid arguments too.
+ */
+size_t sgemm_workspace_size(int variant, int64_t M, int64_t N, int64_t K);
+
+/*
+ * Reads, then clears, the device status word of the current device after
+ * synchronising `stream`: SGEMM_OK, or SGEMM_ERR_TIMEOUT if a kernel gave up
+ * waiting since the last query.  *detail (may be NULL) receives a code that
+ * says which wait expired (0 when none).
+ */
+sgemm_status_t sgemm_query_device_status(cudaStream_t stream, uint32_t *detail);
+
+/* Frees every cached workspace of every device (synchronises the device first). */
+void sgemm_release_workspaces(void);
+
+/* Static description of a status code; never NULL. */
+const char *sgemm_status_string(sgemm_status_t status);
+
+/* Variant name ("guarded", "tiled", ...), or "unknown". */
+const char *sgemm_variant_name(int variant);
+
+/*
+ * Test hook for the timeout path: launches one CTA that waits, with the
+ * library's bounded wait and a limit of `limit_ns` nanoseconds, on a
+ * shared-memory barrier nothing will ever complete.  The kernel records
+ * SGEMM_ERR_TIMEOUT and returns; nothing hangs and no fault is raised.
+ */
+sgemm_status_t sgemm_debug_expire_wait(uint64_t limit_ns, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GB300_SGEMM_H */

@@ -1,0 +1,93 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+* the library builds, loads and exports every function ``include/sgemm.h``
+  declares;
+* argument validation rejects bad calls before touching the device: these
+  paths return their status without any CUDA call, so they run on CPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from dense_fp32_gemm_03_gb300 import _build, binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return binding.load()
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names.update(re.findall(r"\b(sgemm\w*)\s*\(", text))
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    assert {"sgemm", "sgemm_variant", "sgemm_select_variant", "sgemm_query_device_status",
+            "sgemm_status_string"} <= names
+    assert names == set(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"libsgemm.so does not export {name}"
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_and_variant_names(lib):
+    assert binding.status_string(binding.OK) == "ok"
+    assert "invalid" in binding.status_string(binding.ERR_INVALID_VALUE)
+    assert "time" in binding.status_string(binding.ERR_TIMEOUT)
+    assert binding.status_string(99) == "unknown status"
+    for name, v in binding.VARIANTS.items():
+        assert binding.variant_name(v) == name
+    assert binding.variant_name(42) == "unknown"
+
+
+# Fake device addresses: validation fails before any of them is dereferenced.
+P_A, P_B, P_C = 0x10000000, 0x20000000, 0x30000000
+
+
+@pytest.mark.parametrize("args", [
+    (-1, 4, 4, P_A, 4, P_B, 4, P_C, 4),      # negative M
+    (4, -1, 4, P_A, 4, P_B, 4, P_C, 4),      # negative N
+    (4, 4, -1, P_A, 4, P_B, 4, P_C, 4),      # negative K
+    (4, 4, 8, P_A, 7, P_B, 4, P_C, 4),       # lda < K
+    (4, 8, 4, P_A, 4, P_B, 7, P_C, 8),       # ldb < N
+    (4, 8, 4, P_A, 4, P_B, 8, P_C, 7),       # ldc < N
+    (4, 4, 4, 0, 4, P_B, 4, P_C, 4),         # null A
+    (4, 4, 4, P_A, 4, 0, 4, P_C, 4),         # null B
+    (4, 4, 4, P_A, 4, P_B, 4, 0, 4),         # null C
+    (4, 4, 4, P_A, 4, P_B, 4, P_A + 16, 4),  # C overlaps A
+    (4, 4, 4, P_A, 4, P_B, 4, P_B + 60, 4),  # C overlaps B's last element
+])
+def test_invalid_arguments_rejected(lib, args):
+    assert binding.sgemm_raw(*args) == binding.ERR_INVALID_VALUE
+    assert lib.sgemm_select_variant(*args) == -1
+
+
+def test_unknown_variant_rejected(lib):
+    assert binding.sgemm_raw(4, 4, 4, P_A, 4, P_B, 4, P_C, 4, variant=7) in (
+        binding.ERR_INVALID_VALUE, binding.ERR_UNSUPPORTED)
+
+
+def test_oversized_dimension_unsupported(lib):
+    big = 2 ** 31
+    assert binding.sgemm_raw(big, 4, 4, P_A, 4, P_B, 4, P_C, 4) == binding.ERR_UNSUPPORTED
+
+
+def test_null_pointers_allowed_for_empty_extents(lib):
+    """M == 0 or N == 0 is a no-op; K == 0 needs only C.  Validation accepts them
+    (they then need a device, so only the validator is exercised here)."""
+    assert lib.sgemm_workspace_size(binding.STREAMK, 0, 4, 4) == 0
