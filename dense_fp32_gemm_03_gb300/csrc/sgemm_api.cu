@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -24,7 +25,7 @@ using gb300::TileShape;
 __device__ uint32_t g_status_word[2];
 
 constexpr int64_t kInt32Max = 0x7fffffffLL;
-constexpr uint64_t kDefaultWaitLimitNs = 4000000000ull;  // 4 s: far above any legitimate wait
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
 constexpr int kGroupM = 8;
 constexpr int kMinSkIters = 4;  // Stream-K shares shorter than this many k-tiles are not worth splitting
 // Every workspace starts with a counter region of fixed size, so that a cached
@@ -41,7 +42,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 struct DeviceState {
   sgemm_status_t init_status = SGEMM_OK;
   int sms = 0;
-  int ctas_per_sm[gb300::kTileConfigs] = {0, 0};
+  int ctas_per_sm[gb300::kTileConfigs] = {};
   uint32_t* status = nullptr;
 };
 
@@ -49,6 +50,20 @@ struct Workspace {
   void* ptr = nullptr;
   size_t bytes = 0;
 };
+
+// Compiled tile configuration behind each tile size of the variants; the
+// environment variables SGEMM_TILE_LARGE / SGEMM_TILE_SMALL (a configuration
+// id) override them, for tuning sweeps.
+int g_cfg_large = 0;
+int g_cfg_small = 1;
+
+int env_config(const char* name, int fallback) {
+  const char* v = std::getenv(name);
+  if (v == nullptr || *v == 0) return fallback;
+  char* end = nullptr;
+  long id = std::strtol(v, &end, 10);
+  return (end && *end == 0 && id >= 0 && id < gb300::kTileConfigs) ? int(id) : fallback;
+}
 
 std::mutex g_mu;
 std::map<int, DeviceState> g_devices;
@@ -70,6 +85,8 @@ sgemm_status_t device_state(DeviceState** out, int* dev_out) {
       st.init_status = SGEMM_ERR_UNSUPPORTED;  // the library carries sm_103a code only
     } else {
       cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev);
+      g_cfg_large = env_config("SGEMM_TILE_LARGE", g_cfg_large);
+      g_cfg_small = env_config("SGEMM_TILE_SMALL", g_cfg_small);
       for (int c = 0; c < gb300::kTileConfigs; ++c) {
         st.ctas_per_sm[c] = gb300::tile_kernel_prepare(TileConfig(c));
         if (st.ctas_per_sm[c] <= 0) st.init_status = SGEMM_ERR_LAUNCH;
@@ -134,7 +151,7 @@ bool fast_path_ok(const float* A, int64_t lda, const float* B, int64_t ldb, cons
 
 struct Plan {
   int variant = -1;
-  TileConfig cfg = gb300::kTileLarge;
+  TileConfig cfg = 0;
   Sched sc{};
   int grid = 0;
   size_t partial_bytes = 0;
@@ -151,8 +168,8 @@ bool make_plan(int variant, int64_t M, int64_t N, int64_t K, const DeviceState& 
   p->variant = variant;
   if (!is_fast(variant)) return true;
   p->cfg = (variant == SGEMM_VARIANT_TILED_SMALL || variant == SGEMM_VARIANT_STREAMK_SMALL)
-               ? gb300::kTileSmall
-               : gb300::kTileLarge;
+               ? g_cfg_small
+               : g_cfg_large;
   const TileShape ts = gb300::tile_shape(p->cfg);
   const int64_t tiles_m = (M + ts.bm - 1) / ts.bm, tiles_n = (N + ts.bn - 1) / ts.bn;
   const int64_t tiles = tiles_m * tiles_n;
@@ -283,16 +300,28 @@ sgemm_status_t run(int variant, int64_t M, int64_t N, int64_t K, const float* A,
   if (!make_plan(variant, M, N, K, *ds, &p)) return SGEMM_ERR_UNSUPPORTED;
   const TileShape ts = gb300::tile_shape(p.cfg);
 
-  CUtensorMap tmap;
-  std::memset(&tmap, 0, sizeof(tmap));
-  const cuuint64_t dims[2] = {cuuint64_t(N), cuuint64_t(K)};
-  const cuuint64_t strides[1] = {cuuint64_t(ldb) * 4};
-  const cuuint32_t box[2] = {cuuint32_t(ts.bn), cuuint32_t(ts.bk)};
+  CUtensorMap tmap_a, tmap_b;
+  std::memset(&tmap_a, 0, sizeof(tmap_a));
+  std::memset(&tmap_b, 0, sizeof(tmap_b));
   const cuuint32_t estr[2] = {1, 1};
-  if (g_encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(B), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return SGEMM_ERR_LAUNCH;
+  {
+    const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(M)};
+    const cuuint64_t strides[1] = {cuuint64_t(lda) * 4};
+    const cuuint32_t box[2] = {cuuint32_t(ts.bk), cuuint32_t(ts.a_box_rows)};
+    if (g_encode(&tmap_a, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(A), dims, strides,
+                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return SGEMM_ERR_LAUNCH;
+  }
+  {
+    const cuuint64_t dims[2] = {cuuint64_t(N), cuuint64_t(K)};
+    const cuuint64_t strides[1] = {cuuint64_t(ldb) * 4};
+    const cuuint32_t box[2] = {cuuint32_t(ts.bn), cuuint32_t(ts.bk)};
+    if (g_encode(&tmap_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(B), dims, strides,
+                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return SGEMM_ERR_LAUNCH;
+  }
 
   void* ws = nullptr;
   st = get_workspace(dev, stream, p, &ws);
@@ -309,7 +338,7 @@ sgemm_status_t run(int variant, int64_t M, int64_t N, int64_t K, const float* A,
   args.partials = ws ? reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes) : nullptr;
   args.status = ds->status;
   args.wait_limit_ns = kDefaultWaitLimitNs;
-  return gb300::launch_tile_kernel(p.cfg, tmap, args, p.sc, p.grid, stream) == cudaSuccess
+  return gb300::launch_tile_kernel(p.cfg, tmap_a, tmap_b, args, p.sc, p.grid, stream) == cudaSuccess
              ? SGEMM_OK
              : SGEMM_ERR_LAUNCH;
 }

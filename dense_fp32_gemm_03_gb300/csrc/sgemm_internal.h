@@ -49,12 +49,14 @@ struct GemmArgs {
   uint64_t wait_limit_ns;
 };
 
-// Tile configurations of the pipelined kernel.
-enum TileConfig : int { kTileLarge = 0, kTileSmall = 1, kTileConfigs = 2 };
+// Tile configurations of the pipelined kernel (compiled instances, by id).
+typedef int TileConfig;
+constexpr int kTileConfigs = 6;
 
 struct TileShape {
   int bm, bn, bk, threads, stages;
   size_t smem_bytes;
+  int a_box_rows;  // rows of A per TMA copy (one producer warp's slice)
 };
 
 TileShape tile_shape(TileConfig cfg);
@@ -63,8 +65,11 @@ TileShape tile_shape(TileConfig cfg);
 // returns the resident CTAs per SM, or a negative value on error.
 int tile_kernel_prepare(TileConfig cfg);
 
-cudaError_t launch_tile_kernel(TileConfig cfg, const CUtensorMap& tmap_b, const GemmArgs& args,
-                               const Sched& sched, int grid, cudaStream_t stream);
+// tmap_a: A as a 2-D tensor (K fastest) with box {16, a_box_rows} and the
+// 64-byte swizzle; tmap_b: B (N fastest) with box {BN, 16}, no swizzle.
+cudaError_t launch_tile_kernel(TileConfig cfg, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                               const GemmArgs& args, const Sched& sched, int grid,
+                               cudaStream_t stream);
 
 cudaError_t launch_guarded_kernel(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
                                   const float* B, int64_t ldb, float* C, int64_t ldc,

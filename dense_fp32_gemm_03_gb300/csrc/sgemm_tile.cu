@@ -1,35 +1,39 @@
-// sgemm_tile.cu -- the pipelined FP32 GEMM kernel for sm_103a.
+// sgemm_tile.cu -- the warp-specialized FP32 GEMM kernel for sm_103a.
 //
 // C = A * B, row-major FP32, alpha = 1, beta = 0 ("Beyond Kernel 7: Closing
 // the Gap to cuBLAS on an H100 FP32 GEMM", section "The operation").  One
-// kernel template serves three schedules (see Sched in sgemm_internal.h):
-// one tile per CTA, persistent whole-tile waves, and Stream-K splits of K.
+// kernel template serves three schedules (Sched in sgemm_internal.h): one
+// tile per CTA, persistent whole-tile waves, and Stream-K splits of K.
 //
-// Per CTA and output tile BM x BN:
-//  * B (K x N) streams global -> shared through a STAGES-deep ring filled by
-//    TMA (cp.async.bulk.tensor) and guarded by one mbarrier per stage.  The
-//    ring is the multi-stage pipeline of "Beyond Kernel 7", section "Kernel 8:
-//    asynchronous copies", with the bulk tensor copy engine in place of
-//    per-thread cp.async.
-//  * A (M x K) is read with 128-bit loads one k-tile ahead into registers
-//    ("Vectorized Memory Access ...", sections 1 and 3) and written to shared
-//    memory transposed, k-major ([k][m], section 4 of the same page), with
-//    every value stored twice side by side so that a 128-bit shared load
-//    yields ready-made operand pairs (a, a) for the paired FMA.
-//  * Each thread owns an 8 x 16 patch of C (128 accumulators; the 16 x 8 /
-//    8 x 16 patches of "Beyond Kernel 7", section "Kernel 10"), updated per
-//    k step as a register outer product ("2D Block Tiling ...", section 4)
-//    with fma.rn.f32x2: one instruction performs two FP32 FFMAs, each with
-//    its own single rounding, which halves the issue slots the arithmetic
-//    takes and leaves room for the shared loads and address math that bound
-//    the pages' kernels (same page, "Kernel 11" and the closing roofline).
-//  * Warp tiling ("Beyond Kernel 7", section "Kernel 6"): a warp covers
-//    32 x 128 outputs as a 4 x 8 lane grid; within a patch the column quads
-//    are strided by 32 so that the eight lanes of a row read 128 contiguous
-//    bytes of B (conflict-free; "Kernel 10", strided B-column mapping) and
-//    the four lanes of a column read 64 contiguous bytes of A (broadcast).
-//  * Output: coalesced 128-bit row stores ("cuSgemm", Kernel 5), bounds
-//    checked on edge tiles ("2D Block Tiling ...", section 5).
+// Roles inside a CTA:
+//  * a producer warpgroup (four warps, one per SM sub-partition) moves data.
+//    One lane issues TMA bulk-tensor copies (cp.async.bulk.tensor) of B tiles
+//    straight into a STAGES-deep ring.  Each producer warp copies its own
+//    32-row slice of every A tile into a private staging ring laid out with
+//    the 64-byte swizzle, then rewrites it transposed (k-major, "Vectorized
+//    Memory Access ...", section 4) with every value stored twice side by
+//    side, so that one 128-bit shared load yields ready-made operand pairs
+//    (a, a) for the paired FMA.  This is the multi-stage copy pipeline of
+//    "Beyond Kernel 7", section "Kernel 8", with the bulk copy engine in
+//    place of per-thread cp.async; A never passes through the compute warps'
+//    registers or the L1 request path.  The producers give most of their
+//    registers to the consumers (setmaxnreg).
+//  * the consumer warps compute.  Each thread owns an 8 x 16 (or 8 x 8)
+//    patch of C ("Beyond Kernel 7", section "Kernel 10"), updated per k step
+//    as a register outer product ("2D Block Tiling ...", section 4) with
+//    fma.rn.f32x2: one instruction performs two FP32 FFMAs, each with its own
+//    single rounding, halving the issue slots the arithmetic takes.
+//  Producers and consumers meet only at per-stage mbarriers ("full": the
+//  stage holds data; "empty": every consumer warp is done with it), so the
+//  compute loop has no block-wide barrier.
+//
+// Warp tiling ("Beyond Kernel 7", section "Kernel 6"): a consumer warp covers
+// 32 x (8 * TN) outputs as a 4 x 8 lane grid; within a patch the column
+// quads are strided by 32 so that the eight lanes of a row read 128
+// contiguous bytes of B ("Kernel 10", strided B-column mapping) and the four
+// lanes of a column read 64 contiguous bytes of A.  Output: coalesced
+// 128-bit row stores ("cuSgemm", Kernel 5), bounds-checked on edge tiles
+// ("2D Block Tiling ...", section 5).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -41,37 +45,137 @@ namespace {
 
 constexpr uint32_t kStatusTimeout = 3;  // SGEMM_ERR_TIMEOUT
 
-template <int WARPS_M, int WARPS_N, int BK_, int STAGES, int MIN_CTAS>
+template <int WARPS_M, int WARPS_N, int TN, int STAGES, int ASTAGES, bool DB, int CTAS>
 struct TileCfg {
-  static constexpr int kTR = 4, kTC = 8;    // lane grid of a warp: rows x columns
-  static constexpr int kTM = 8, kTN = 16;   // outputs per thread
+  static constexpr int kTR = 4, kTC = 8;    // lane grid of a consumer warp: rows x columns
+  static constexpr int kTM = 8, kTN = TN;   // outputs per thread
   static constexpr int kWarpM = kTR * kTM;  // 32
-  static constexpr int kWarpN = kTC * kTN;  // 128
+  static constexpr int kWarpN = kTC * kTN;  // 64 or 128
   static constexpr int kWarpsM = WARPS_M;
+  static constexpr int kConsumerWarps = WARPS_M * WARPS_N;
+  static constexpr int kConsumers = 32 * kConsumerWarps;
+  static constexpr int kProducerWarps = 4;  // one warpgroup: one warp per SM sub-partition
+  static constexpr int kProducers = 32 * kProducerWarps;
+  static constexpr int NT = kConsumers + kProducers;
+  static constexpr int kCtasPerSm = CTAS;
+  // Registers: the launch gives every thread R0; the producer warpgroup then
+  // hands registers to the consumer warpgroups (setmaxnreg), keeping the total.
+  static constexpr int kRegsLaunch = (65536 / (CTAS * NT)) / 8 * 8;
+  static constexpr int kRegsProducer = 56;
+  static constexpr int kRegsConsumer =
+      ((NT * kRegsLaunch - kProducers * kRegsProducer) / kConsumers) / 8 * 8;
   static constexpr int BM = WARPS_M * kWarpM;
   static constexpr int BN = WARPS_N * kWarpN;
-  static constexpr int BK = BK_;
+  static constexpr int BK = 16;  // one 64-byte swizzle span of A per row
+  static constexpr int kRowsPerProducer = BM / kProducerWarps;  // 32
   static constexpr int S = STAGES;
-  static constexpr int NT = 32 * WARPS_M * WARPS_N;
-  static constexpr int kMinCtas = MIN_CTAS;
+  static constexpr int S2 = ASTAGES;
+  static constexpr bool kDoubleBuffer = DB;
   static constexpr int kAStride = 2 * BM;  // floats per k row of the doubled, transposed A tile
-  static constexpr int kABufFloats = BK * kAStride;
+  static constexpr int kAStageFloats = BK * kAStride;
   static constexpr int kBStageFloats = BK * BN;
+  static constexpr int kAStagingFloats = kRowsPerProducer * BK;  // one producer warp's slot
   static constexpr uint32_t kBStageBytes = kBStageFloats * 4;
-  static constexpr int kAVec = BM * BK / (4 * NT);  // 128-bit A loads per thread per k-tile
-  static constexpr int kOutVec = kTM * kTN / 4;     // float4 partial values per thread
+  static constexpr uint32_t kAStagingBytes = kAStagingFloats * 4;
+  static constexpr int kOutVec = kTM * kTN / 4;  // float4 values per thread
+  // Shared memory: [B ring][A staging: producer warp x slot][A ring][barriers][flags]
   static constexpr size_t kBOff = 0;
-  static constexpr size_t kAOff = S * size_t(kBStageBytes);
-  static constexpr size_t kBarOff = kAOff + 2 * size_t(kABufFloats) * 4;
-  static constexpr size_t kFlagOff = kBarOff + S * 8;
+  static constexpr size_t kAStagingOff = kBOff + size_t(S) * kBStageBytes;
+  static constexpr size_t kAOff = kAStagingOff + size_t(kProducerWarps) * S2 * kAStagingBytes;
+  static constexpr size_t kBarOff = kAOff + size_t(S) * kAStageFloats * 4;
+  static constexpr size_t kFlagOff = kBarOff + size_t(2 * S + kProducerWarps * S2) * 8;
   static constexpr size_t kSmem = kFlagOff + 16;
-  static_assert(NT % BM == 0 && (NT / BM) * kAVec * 4 == BK, "A load split must cover the tile");
-  static_assert(BN <= 256 && BK <= 256, "TMA box dimensions are at most 256");
-  static_assert((S & (S - 1)) == 0, "stage count must be a power of two");
+  static_assert(TN == 8 || TN == 16, "patch width");
+  static_assert(kRowsPerProducer == 32, "each producer lane owns one row of the A tile");
+  static_assert(BM <= 256 && BN <= 256, "TMA box dimensions are at most 256");
+  static_assert(kBStageBytes % 1024 == 0 && kAStagingBytes % 512 == 0,
+                "stages keep the 64-byte swizzle period (512 bytes) aligned");
+  static_assert(kConsumers * kRegsConsumer + kProducers * kRegsProducer <= NT * kRegsLaunch,
+                "register hand-over must stay within the launch allocation");
+  static_assert(kRegsConsumer <= 256 && kRegsConsumer >= kRegsLaunch, "consumer register budget");
 };
 
-using CfgLarge = TileCfg<4, 2, 16, 4, 1>;  // 128 x 256 tile, 256 threads, 1 CTA / SM
-using CfgSmall = TileCfg<4, 1, 8, 8, 2>;   // 128 x 128 tile, 128 threads, 2 CTAs / SM
+// The compiled tile configurations (index = TileConfig id).
+using Cfg0 = TileCfg<4, 2, 16, 4, 4, false, 1>;  // 128 x 256 tile, 8 + 4 warps, 8x16 patch
+using Cfg1 = TileCfg<4, 1, 16, 4, 4, false, 2>;  // 128 x 128 tile, 4 + 4 warps, 2 CTAs / SM
+using Cfg2 = TileCfg<4, 2, 16, 6, 4, false, 1>;  // Cfg0 with a deeper ring
+using Cfg3 = TileCfg<4, 2, 8, 4, 4, true, 1>;    // 128 x 128 tile, 8 + 4 warps, 8x8 patch
+using Cfg4 = TileCfg<4, 2, 16, 3, 3, false, 1>;  // Cfg0 with a shallower ring
+using Cfg5 = TileCfg<4, 1, 16, 3, 3, false, 2>;  // Cfg1 with a shallower ring
+
+template <class F>
+auto with_cfg(int id, F&& f) {
+  switch (id) {
+    case 1: return f(Cfg1{});
+    case 2: return f(Cfg2{});
+    case 3: return f(Cfg3{});
+    case 4: return f(Cfg4{});
+    case 5: return f(Cfg5{});
+    default: return f(Cfg0{});
+  }
+}
+
+// One unit of work: a tile and a range [kb, ke) of its k-tiles.
+struct Unit {
+  int tile, kb, ke, t_sk;  // t_sk >= 0: index of a split (Stream-K) tile
+};
+
+// Walks the units of one CTA: whole tiles first, then its Stream-K share.
+struct WorkIter {
+  int dp_next;
+  int64_t sk_pos, sk_end;
+
+  __device__ __forceinline__ void init(const Sched& sc, int cta) {
+    dp_next = cta;
+    sk_pos = sk_end = 0;
+    if (sc.sk_tiles > 0 && cta < sc.sk_ctas) {
+      sk_pos = int64_t(cta) * sc.sk_base + min(cta, sc.sk_extra);
+      sk_end = sk_pos + sc.sk_base + (cta < sc.sk_extra ? 1 : 0);
+    }
+  }
+
+  __device__ __forceinline__ bool next(const Sched& sc, int ctas, Unit& u) {
+    if (dp_next < sc.dp_tiles) {
+      u.tile = dp_next;
+      u.kb = 0;
+      u.ke = sc.iters_per_tile;
+      u.t_sk = -1;
+      dp_next += ctas;
+      return true;
+    }
+    if (sk_pos < sk_end) {
+      u.t_sk = int(sk_pos / sc.iters_per_tile);
+      const int64_t start = int64_t(u.t_sk) * sc.iters_per_tile;
+      u.kb = int(sk_pos - start);
+      const int64_t left = sk_end - start;
+      u.ke = left < sc.iters_per_tile ? int(left) : sc.iters_per_tile;
+      u.tile = sc.dp_tiles + u.t_sk;
+      sk_pos = start + u.ke;
+      return true;
+    }
+    return false;
+  }
+};
+
+// Walks the k-tiles of all units of one CTA in order.
+struct KCursor {
+  WorkIter w;
+  Unit u;
+  int j;
+  bool valid;
+
+  __device__ __forceinline__ void init(const Sched& sc, int cta, int ctas) {
+    w.init(sc, cta);
+    j = 0;
+    valid = w.next(sc, ctas, u);
+  }
+  __device__ __forceinline__ void advance(const Sched& sc, int ctas) {
+    if (++j >= u.ke - u.kb) {
+      j = 0;
+      valid = w.next(sc, ctas, u);
+    }
+  }
+};
 
 // Maps a linear tile index to (tile row, tile column) in groups of `group_m`
 // tile rows, so that CTAs running together share panels of A and B in L2
@@ -95,67 +199,151 @@ __device__ __forceinline__ int sk_owner(const Sched& sc, int64_t i) {
 }
 
 template <class T>
-__global__ void __launch_bounds__(T::NT, T::kMinCtas)
-    tile_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs args, const Sched sc) {
+__global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
+    tile_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                const GemmArgs args, const Sched sc) {
   extern __shared__ __align__(1024) unsigned char smem[];
   float* sB = reinterpret_cast<float*>(smem + T::kBOff);
+  float* sAst = reinterpret_cast<float*>(smem + T::kAStagingOff);
   float* sA = reinterpret_cast<float*>(smem + T::kAOff);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + T::kBarOff);
-  int& s_last = *reinterpret_cast<int*>(smem + T::kFlagOff);
+  uint64_t* empty = full + T::S;
+  uint64_t* astage = empty + T::S;  // [producer warp][slot]
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + T::kFlagOff);
+  int* s_last = reinterpret_cast<int*>(smem + T::kFlagOff + 4);
 
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
-  const int tr = lane / T::kTC, tc = lane % T::kTC;
-  const int wm = warp % T::kWarpsM, wn = warp / T::kWarpsM;
-  // Compute-side shared-memory offsets (floats).
-  const int a_frag = 2 * wm * T::kWarpM + 4 * tr;  // + 16 g + kAStride kk
-  const int b_frag = wn * T::kWarpN + 4 * tc;      // + 32 h + BN kk
-  // Load-side assignment for A: one row, kAVec consecutive 4-wide k groups.
-  const int a_row = tid % T::BM;
-  const int a_q0 = (tid / T::BM) * T::kAVec;
+  const int cta = blockIdx.x, ctas = gridDim.x;
+  const uint64_t limit = args.wait_limit_ns;
 
   if (tid == 0) {
-#pragma unroll
-    for (int s = 0; s < T::S; ++s) dev::mbar_init(&full[s], 1);
+    for (int s = 0; s < T::S; ++s) {
+      dev::mbar_init(&full[s], T::kProducers);       // every producer thread
+      dev::mbar_init(&empty[s], T::kConsumerWarps);  // one arrival per consumer warp
+    }
+    for (int s = 0; s < T::kProducerWarps * T::S2; ++s) dev::mbar_init(&astage[s], 1);
+    *s_abort = 0;
     dev::mbar_init_fence();
-    dev::tma_prefetch_desc(&tmap_b);
   }
   __syncthreads();
 
-  const int M = args.M, N = args.N, K = args.K;
-  const int cta = blockIdx.x, ctas = gridDim.x;
-  uint32_t it = 0;  // k-tiles this CTA has consumed: position in the stage ring
+  // A wait that failed: record it once, make every later wait of the CTA give
+  // up at once, and carry on without waiting so that nothing hangs.
+  auto fail = [&](uint32_t site) {
+    if (!*s_abort) {
+      *s_abort = 1;
+      dev::record_status(args.status, kStatusTimeout, site);
+    }
+  };
 
-  // Work list of this CTA: whole tiles first, then its Stream-K iterations.
-  int dp_next = cta;
-  int64_t sk_pos = 0, sk_end = 0;
-  if (sc.sk_tiles > 0 && cta < sc.sk_ctas) {
-    sk_pos = int64_t(cta) * sc.sk_base + min(cta, sc.sk_extra);
-    sk_end = sk_pos + sc.sk_base + (cta < sc.sk_extra ? 1 : 0);
+  if (warp >= T::kConsumerWarps) {
+    // ================================================ producer warpgroup
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(T::kRegsProducer));
+    const int pw = warp - T::kConsumerWarps;  // this warp owns A rows [32 pw, 32 pw + 32)
+    uint64_t* my_astage = astage + pw * T::S2;
+    float* my_staging = sAst + pw * T::S2 * T::kAStagingFloats;
+    if (lane == 0) {
+      dev::tma_prefetch_desc(&tmap_a);
+      if (pw == 0) dev::tma_prefetch_desc(&tmap_b);
+    }
+    KCursor issue, proc;
+    issue.init(sc, cta, ctas);
+    proc.init(sc, cta, ctas);
+    auto tile_mn = [&](const Unit& u, int& m0, int& n0) {
+      int tm, tn;
+      tile_coords(sc, u.tile, tm, tn);
+      m0 = tm * T::BM;
+      n0 = tn * T::BN;
+    };
+    auto issue_a = [&](uint32_t slot) {
+      int m0, n0;
+      tile_mn(issue.u, m0, n0);
+      dev::mbar_arrive_expect_tx(&my_astage[slot], T::kAStagingBytes);
+      dev::tma_load_2d(my_staging + slot * T::kAStagingFloats, &tmap_a,
+                       (issue.u.kb + issue.j) * T::BK, m0 + pw * T::kRowsPerProducer,
+                       &my_astage[slot]);
+    };
+    // Prologue: this warp's first S2 A slices into its staging ring.
+    uint32_t issued = 0;
+    for (int s = 0; s < T::S2 && issue.valid; ++s) {
+      if (lane == 0) issue_a(s);
+      ++issued;
+      issue.advance(sc, ctas);
+    }
+    uint32_t i = 0;
+    for (; proc.valid; ++i) {
+      const uint32_t s = i % T::S, n = i / T::S;
+      const uint32_t s2 = i % T::S2, n2 = i / T::S2;
+      if (n > 0 && !dev::mbar_wait_abortable(&empty[s], (n - 1) & 1u, limit, s_abort))
+        fail(kWaitTileStage);
+      if (pw == 0 && lane == 0 && !*s_abort) {
+        int m0, n0;
+        tile_mn(proc.u, m0, n0);
+        dev::mbar_expect_tx(&full[s], T::kBStageBytes);
+        dev::tma_load_2d(sB + s * T::kBStageFloats, &tmap_b, n0, (proc.u.kb + proc.j) * T::BK,
+                         &full[s]);
+      }
+      if (!dev::mbar_wait_abortable(&my_astage[s2], n2 & 1u, limit, s_abort)) fail(kWaitTileStage);
+      // Transpose and double this warp's 32 rows: staging [r][k] (64-byte
+      // swizzled rows: 16-byte chunk q of row r sits at q ^ ((r >> 1) & 3))
+      // -> ring [k][2m].
+      {
+        const int r = lane;                    // row within this warp's slice
+        const int m = pw * T::kRowsPerProducer + r;  // row within the tile
+        const float* src = my_staging + s2 * T::kAStagingFloats + r * T::BK;
+        float* d = sA + s * T::kAStageFloats + 2 * m;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 v = *reinterpret_cast<const float4*>(src + (q ^ ((r >> 1) & 3)) * 4);
+          *reinterpret_cast<float2*>(d + (4 * q + 0) * T::kAStride) = make_float2(v.x, v.x);
+          *reinterpret_cast<float2*>(d + (4 * q + 1) * T::kAStride) = make_float2(v.y, v.y);
+          *reinterpret_cast<float2*>(d + (4 * q + 2) * T::kAStride) = make_float2(v.z, v.z);
+          *reinterpret_cast<float2*>(d + (4 * q + 3) * T::kAStride) = make_float2(v.w, v.w);
+        }
+      }
+      __syncwarp();
+      // The staging slot is free again: refill it with the slice S2 k-tiles ahead.
+      if (issue.valid) {
+        if (lane == 0 && !*s_abort) {
+          dev::fence_proxy_async_smem();
+          issue_a(s2);
+        }
+        ++issued;
+        issue.advance(sc, ctas);
+      }
+      dev::mbar_arrive(&full[s]);
+      proc.advance(sc, ctas);
+    }
+    // Normally every copy was consumed.  After a failure, let any copy still
+    // in flight land (bounded) before the CTA's shared memory is released.
+    if (*s_abort && lane == 0) {
+      for (uint32_t k = i; k < issued; ++k)
+        dev::mbar_wait(&my_astage[k % T::S2], (k / T::S2) & 1u, limit);
+      if (pw == 0)
+        for (uint32_t k = (i > T::S ? i - T::S : 0); k < i; ++k)
+          dev::mbar_wait(&full[k % T::S], (k / T::S) & 1u, limit);
+    }
+    return;
   }
 
-  for (;;) {
-    int tile, kb, ke, t_sk = -1;
-    if (dp_next < sc.dp_tiles) {
-      tile = dp_next;
-      kb = 0;
-      ke = sc.iters_per_tile;
-      dp_next += ctas;
-    } else if (sk_pos < sk_end) {
-      t_sk = int(sk_pos / sc.iters_per_tile);
-      const int64_t tile_start = int64_t(t_sk) * sc.iters_per_tile;
-      kb = int(sk_pos - tile_start);
-      const int64_t left = sk_end - tile_start;
-      ke = left < sc.iters_per_tile ? int(left) : sc.iters_per_tile;
-      tile = sc.dp_tiles + t_sk;
-      sk_pos = tile_start + ke;
-    } else {
-      break;
-    }
+  // ======================================================= consumer warps
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(T::kRegsConsumer));
+  const int tr = lane / T::kTC, tc = lane % T::kTC;
+  const int wm = warp % T::kWarpsM, wn = warp / T::kWarpsM;
+  const int a_frag = 2 * wm * T::kWarpM + 4 * tr;  // + 16 g + kAStride kk
+  const int b_frag = wn * T::kWarpN + 4 * tc;      // + 32 h + BN kk
+  const int M = args.M, N = args.N;
+
+  WorkIter w;
+  w.init(sc, cta);
+  Unit u;
+  uint32_t it = 0;  // k-tiles consumed so far: position in the stage ring
+  while (w.next(sc, ctas, u)) {
     int tm, tn;
-    tile_coords(sc, tile, tm, tn);
+    tile_coords(sc, u.tile, tm, tn);
     const int m0 = tm * T::BM, n0 = tn * T::BN;
-    const int nk = ke - kb;
+    const int nk = u.ke - u.kb;
 
     float2 acc[T::kTM][T::kTN / 2];
 #pragma unroll
@@ -163,113 +351,72 @@ __global__ void __launch_bounds__(T::NT, T::kMinCtas)
 #pragma unroll
       for (int q = 0; q < T::kTN / 2; ++q) acc[r][q] = make_float2(0.f, 0.f);
 
-    // ---- prologue: fill the B ring, stage the first A tile
-    if (tid == 0) {
-      for (int j = 0; j < T::S && j < nk; ++j) {
-        const uint32_t st = (it + j) & (T::S - 1);
-        dev::mbar_arrive_expect_tx(&full[st], T::kBStageBytes);
-        dev::tma_load_2d(sB + st * T::kBStageFloats, &tmap_b, n0, (kb + j) * T::BK, &full[st]);
-      }
-    }
-    const int a_grow = m0 + a_row;
-    const bool a_row_ok = a_grow < M;
-    const float* a_src = args.A + int64_t(a_row_ok ? a_grow : 0) * args.lda + a_q0 * 4;
-    float4 areg[T::kAVec];
-    auto load_a = [&](int kt) {
-      const int k0 = kt * T::BK + a_q0 * 4;
-#pragma unroll
-      for (int v = 0; v < T::kAVec; ++v) {
-        const int k = k0 + 4 * v;
-        const float* p = a_src + int64_t(kt) * T::BK + 4 * v;
-        if (a_row_ok && k + 4 <= K) {
-          areg[v] = __ldg(reinterpret_cast<const float4*>(p));
-        } else {
-          areg[v].x = (a_row_ok && k + 0 < K) ? __ldg(p + 0) : 0.f;
-          areg[v].y = (a_row_ok && k + 1 < K) ? __ldg(p + 1) : 0.f;
-          areg[v].z = (a_row_ok && k + 2 < K) ? __ldg(p + 2) : 0.f;
-          areg[v].w = (a_row_ok && k + 3 < K) ? __ldg(p + 3) : 0.f;
-        }
-      }
-    };
-    auto store_a = [&](int buf) {
-      float* dst = sA + buf * T::kABufFloats + 2 * a_row;
-#pragma unroll
-      for (int v = 0; v < T::kAVec; ++v) {
-        const int kl = (a_q0 + v) * 4;
-        *reinterpret_cast<float2*>(dst + (kl + 0) * T::kAStride) = make_float2(areg[v].x, areg[v].x);
-        *reinterpret_cast<float2*>(dst + (kl + 1) * T::kAStride) = make_float2(areg[v].y, areg[v].y);
-        *reinterpret_cast<float2*>(dst + (kl + 2) * T::kAStride) = make_float2(areg[v].z, areg[v].z);
-        *reinterpret_cast<float2*>(dst + (kl + 3) * T::kAStride) = make_float2(areg[v].w, areg[v].w);
-      }
-    };
-    load_a(kb);
-    store_a(0);
-    __syncthreads();
-
-    // ---- main loop over the k-tiles of this work unit
-    for (int j = 0; j < nk; ++j) {
-      const bool more = j + 1 < nk;
-      if (more) load_a(kb + j + 1);
-      const uint32_t pos = it + j;
-      const uint32_t st = pos & (T::S - 1);
-      const bool ok = dev::mbar_wait(&full[st], (pos / T::S) & 1u, args.wait_limit_ns);
-      const float* a_buf = sA + (j & 1) * T::kABufFloats + a_frag;
-      const float* b_buf = sB + st * T::kBStageFloats + b_frag;
-#pragma unroll
-      for (int kk = 0; kk < T::BK; ++kk) {
-        float4 a4[T::kTM / 2], b4[T::kTN / 4];
+    for (int j = 0; j < nk; ++j, ++it) {
+      const uint32_t s = it % T::S;
+      if (!dev::mbar_wait_abortable(&full[s], (it / T::S) & 1u, limit, s_abort)) fail(kWaitTileStage);
+      const float* a_buf = sA + s * T::kAStageFloats + a_frag;
+      const float* b_buf = sB + s * T::kBStageFloats + b_frag;
+      struct Frag {
+        float4 a[T::kTM / 2];  // (a[m], a[m], a[m+1], a[m+1]) for the thread's row pairs
+        float4 b[T::kTN / 4];  // four consecutive B values per column quad
+      };
+      auto load_frag = [&](Frag& f, int kk) {
 #pragma unroll
         for (int g = 0; g < T::kTM / 2; ++g)
-          a4[g] = *reinterpret_cast<const float4*>(a_buf + kk * T::kAStride + 16 * g);
+          f.a[g] = *reinterpret_cast<const float4*>(a_buf + kk * T::kAStride + 16 * g);
 #pragma unroll
         for (int h = 0; h < T::kTN / 4; ++h)
-          b4[h] = *reinterpret_cast<const float4*>(b_buf + kk * T::BN + 32 * h);
+          f.b[h] = *reinterpret_cast<const float4*>(b_buf + kk * T::BN + 32 * h);
+      };
+      // B-major order: consecutive FFMA2s share one B pair and walk the rows,
+      // which measured markedly faster than row-major orders on sm_103a.
+      auto fma_frag = [&](const Frag& f) {
 #pragma unroll
-        for (int g = 0; g < T::kTM / 2; ++g) {
-          const float2 a_lo = make_float2(a4[g].x, a4[g].y);  // (a[m], a[m])
-          const float2 a_hi = make_float2(a4[g].z, a4[g].w);  // (a[m+1], a[m+1])
+        for (int h = 0; h < T::kTN / 4; ++h) {
 #pragma unroll
-          for (int h = 0; h < T::kTN / 4; ++h) {
-            const float2 b_lo = make_float2(b4[h].x, b4[h].y);
-            const float2 b_hi = make_float2(b4[h].z, b4[h].w);
-            dev::ffma2(acc[2 * g][2 * h], a_lo, b_lo);
-            dev::ffma2(acc[2 * g][2 * h + 1], a_lo, b_hi);
-            dev::ffma2(acc[2 * g + 1][2 * h], a_hi, b_lo);
-            dev::ffma2(acc[2 * g + 1][2 * h + 1], a_hi, b_hi);
+          for (int p = 0; p < 2; ++p) {
+            const float2 bq = p ? make_float2(f.b[h].z, f.b[h].w) : make_float2(f.b[h].x, f.b[h].y);
+#pragma unroll
+            for (int g = 0; g < T::kTM / 2; ++g) {
+              dev::ffma2(acc[2 * g][2 * h + p], make_float2(f.a[g].x, f.a[g].y), bq);
+              dev::ffma2(acc[2 * g + 1][2 * h + p], make_float2(f.a[g].z, f.a[g].w), bq);
+            }
           }
         }
-      }
-      if (more) store_a((j + 1) & 1);
-      if (__syncthreads_or(!ok)) {
-        // A stage never landed: record the timeout, let the copies still in
-        // flight finish (bounded) so none lands after the CTA has exited.
-        if (tid == 0) {
-          for (int jj = j; jj < nk && jj < j + T::S; ++jj) {
-            const uint32_t p2 = it + jj;
-            dev::mbar_wait(&full[p2 & (T::S - 1)], (p2 / T::S) & 1u, args.wait_limit_ns);
-          }
-          dev::record_status(args.status, kStatusTimeout, kWaitTileStage);
+      };
+      if constexpr (T::kDoubleBuffer) {
+        Frag f[2];
+        load_frag(f[0], 0);
+#pragma unroll
+        for (int kk = 0; kk < T::BK; ++kk) {
+          if (kk + 1 < T::BK) load_frag(f[(kk + 1) & 1], kk + 1);
+          fma_frag(f[kk & 1]);
         }
-        return;
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < T::BK; ++kk) {
+          Frag f;
+          load_frag(f, kk);
+          fma_frag(f);
+        }
       }
-      if (tid == 0 && j + T::S < nk) {
-        dev::mbar_arrive_expect_tx(&full[st], T::kBStageBytes);
-        dev::tma_load_2d(sB + st * T::kBStageFloats, &tmap_b, n0, (kb + j + T::S) * T::BK,
-                         &full[st]);
-      }
+      __syncwarp();
+      if (lane == 0) dev::mbar_arrive(&empty[s]);
     }
-    it += nk;
 
     // ---- epilogue
-    // Thread value j (0..31) is the float4 of patch row r = j / 4, column quad h = j % 4.
-    auto out_row = [&](int r) { return m0 + wm * T::kWarpM + (r >> 1) * (2 * T::kTR) + 2 * tr + (r & 1); };
+    // Thread value j is the float4 of patch row r = j / Q, column quad h = j % Q.
+    constexpr int Q = T::kTN / 4;
+    auto out_row = [&](int r) {
+      return m0 + wm * T::kWarpM + (r >> 1) * (2 * T::kTR) + 2 * tr + (r & 1);
+    };
     auto out_col = [&](int h) { return n0 + wn * T::kWarpN + h * (4 * T::kTC) + 4 * tc; };
     auto value = [&](int j) {
-      const int r = j >> 2, h = j & 3;
+      const int r = j / Q, h = j % Q;
       return make_float4(acc[r][2 * h].x, acc[r][2 * h].y, acc[r][2 * h + 1].x, acc[r][2 * h + 1].y);
     };
     auto store_c = [&](int j, float4 v) {
-      const int row = out_row(j >> 2), col = out_col(j & 3);
+      const int row = out_row(j / Q), col = out_col(j % Q);
       if (row >= M) return;
       float* p = args.C + int64_t(row) * args.ldc + col;
       if (col + 4 <= N) {
@@ -282,12 +429,11 @@ __global__ void __launch_bounds__(T::NT, T::kMinCtas)
       }
     };
 
-    const bool whole = (kb == 0 && ke == sc.iters_per_tile);
-    if (whole) {
+    if (u.t_sk < 0 || (u.kb == 0 && u.ke == sc.iters_per_tile)) {
       if (m0 + T::BM <= M && n0 + T::BN <= N) {
 #pragma unroll
         for (int j = 0; j < T::kOutVec; ++j) {
-          float* p = args.C + int64_t(out_row(j >> 2)) * args.ldc + out_col(j & 3);
+          float* p = args.C + int64_t(out_row(j / Q)) * args.ldc + out_col(j % Q);
           *reinterpret_cast<float4*>(p) = value(j);
         }
       } else {
@@ -298,24 +444,26 @@ __global__ void __launch_bounds__(T::NT, T::kMinCtas)
     }
 
     // Split tile: publish this CTA's partial sums; the last CTA to arrive
-    // adds all partials in CTA order and writes C.
-    const int64_t t_first_iter = int64_t(t_sk) * sc.iters_per_tile;
+    // adds all partials in CTA order (deterministic) and writes C.
+    const int64_t t_first_iter = int64_t(u.t_sk) * sc.iters_per_tile;
     const int c_first = sk_owner(sc, t_first_iter);
     const int c_last = sk_owner(sc, t_first_iter + sc.iters_per_tile - 1);
     const int64_t tile_floats = int64_t(T::BM) * T::BN;
     {
-      float4* mine = reinterpret_cast<float4*>(args.partials + (t_sk + cta) * tile_floats);
+      float4* mine = reinterpret_cast<float4*>(args.partials + (u.t_sk + cta) * tile_floats);
 #pragma unroll
-      for (int j = 0; j < T::kOutVec; ++j) __stcg(mine + j * T::NT + tid, value(j));
+      for (int j = 0; j < T::kOutVec; ++j) __stcg(mine + j * T::kConsumers + tid, value(j));
     }
     __threadfence();
-    __syncthreads();
+    dev::named_barrier(1, T::kConsumers);
     if (tid == 0) {
-      const int arrived = atomicAdd(args.counters + t_sk, 1);
-      s_last = (arrived == c_last - c_first) ? 1 : 0;
+      const int arrived = atomicAdd(args.counters + u.t_sk, 1);
+      *s_last = (arrived == c_last - c_first) ? 1 : 0;
     }
-    __syncthreads();
-    if (s_last) {
+    dev::named_barrier(1, T::kConsumers);
+    const bool last = *s_last != 0;
+    dev::named_barrier(1, T::kConsumers);  // s_last may be rewritten by the next split tile
+    if (last) {
       __threadfence();
 #pragma unroll
       for (int j = 0; j < T::kOutVec; ++j) {
@@ -326,20 +474,23 @@ __global__ void __launch_bounds__(T::NT, T::kMinCtas)
           if (cc == cta) {
             v = value(j);
           } else {
-            const float4* src = reinterpret_cast<const float4*>(args.partials + (t_sk + cc) * tile_floats);
-            v = __ldcg(src + j * T::NT + tid);
+            const float4* src =
+                reinterpret_cast<const float4*>(args.partials + (u.t_sk + cc) * tile_floats);
+            v = __ldcg(src + j * T::kConsumers + tid);
           }
           if (cc == c_first) {
             sum = v;
           } else {
-            sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+            sum.x += v.x;
+            sum.y += v.y;
+            sum.z += v.z;
+            sum.w += v.w;
           }
         }
         store_c(j, sum);
       }
-      if (tid == 0) args.counters[t_sk] = 0;
+      if (tid == 0) args.counters[u.t_sk] = 0;
     }
-    // The next unit's prologue rewrites shared memory only after its own barrier.
   }
 }
 
@@ -357,27 +508,27 @@ int prepare() {
 
 template <class T>
 TileShape shape_of() {
-  return TileShape{T::BM, T::BN, T::BK, T::NT, T::S, T::kSmem};
+  return TileShape{T::BM, T::BN, T::BK, T::NT, T::S, T::kSmem, T::kRowsPerProducer};
 }
 
 }  // namespace
 
 TileShape tile_shape(TileConfig cfg) {
-  return cfg == kTileSmall ? shape_of<CfgSmall>() : shape_of<CfgLarge>();
+  return with_cfg(cfg, [](auto c) { return shape_of<decltype(c)>(); });
 }
 
 int tile_kernel_prepare(TileConfig cfg) {
-  return cfg == kTileSmall ? prepare<CfgSmall>() : prepare<CfgLarge>();
+  return with_cfg(cfg, [](auto c) { return prepare<decltype(c)>(); });
 }
 
-cudaError_t launch_tile_kernel(TileConfig cfg, const CUtensorMap& tmap_b, const GemmArgs& args,
-                               const Sched& sched, int grid, cudaStream_t stream) {
-  if (cfg == kTileSmall) {
-    tile_kernel<CfgSmall><<<grid, CfgSmall::NT, CfgSmall::kSmem, stream>>>(tmap_b, args, sched);
-  } else {
-    tile_kernel<CfgLarge><<<grid, CfgLarge::NT, CfgLarge::kSmem, stream>>>(tmap_b, args, sched);
-  }
-  return cudaGetLastError();
+cudaError_t launch_tile_kernel(TileConfig cfg, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                               const GemmArgs& args, const Sched& sched, int grid,
+                               cudaStream_t stream) {
+  return with_cfg(cfg, [&](auto c) {
+    using T = decltype(c);
+    tile_kernel<T><<<grid, T::NT, T::kSmem, stream>>>(tmap_a, tmap_b, args, sched);
+    return cudaGetLastError();
+  });
 }
 
 }  // namespace gb300
