@@ -22,7 +22,7 @@ VARIANTS = {"guarded": GUARDED, "tiled": TILED, "streamk": STREAMK,
 # Every entry point include/sgemm.h declares.
 EXPORTS = ("sgemm", "sgemm_variant", "sgemm_select_variant", "sgemm_workspace_size",
            "sgemm_query_device_status", "sgemm_release_workspaces", "sgemm_status_string",
-           "sgemm_variant_name", "sgemm_debug_expire_wait")
+           "sgemm_variant_name", "sgemm_debug_expire_wait", "sgemm_streamk_static")
 
 
 class SgemmError(RuntimeError):
@@ -72,6 +72,8 @@ def load(path: str | None = None):
         lib.sgemm_variant_name.restype = ctypes.c_char_p
         lib.sgemm_debug_expire_wait.argtypes = [ctypes.c_uint64, vp]
         lib.sgemm_debug_expire_wait.restype = st
+        lib.sgemm_streamk_static.argtypes = gemm_args
+        lib.sgemm_streamk_static.restype = st
         _lib = lib
         return lib
 
@@ -165,6 +167,11 @@ def debug_expire_wait(limit_ns: int, stream=None) -> int:
     import torch
     return load().sgemm_debug_expire_wait(int(limit_ns),
                                           _stream_handle(torch.cuda.current_device(), stream))
+
+
+def sgemm_streamk_static_raw(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    """The allocation-free Stream-K entry point, with integer device addresses."""
+    return load().sgemm_streamk_static(M, N, K, A, lda, B, ldb, C, ldc, stream)
 
 
 def release_workspaces() -> None:

@@ -450,3 +450,108 @@ sgemm_status_t sgemm_debug_expire_wait(uint64_t limit_ns, cudaStream_t stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free Stream-K entry point.
+//
+// The Stream-K schedule needs scratch memory (arrival counters and the
+// partial sums of split tiles).  sgemm() takes it from a cache that calls
+// cudaMalloc the first time a stream needs more.  Some callers cannot let a
+// library allocate: code that runs while its stream is being captured, code
+// that must never wait on the whole device (cudaMalloc and cudaFree may
+// synchronise it), and code that hands out a fixed memory budget before any
+// work starts.  sgemm_streamk_static() serves them from a fixed array in the
+// library's device image instead.
+namespace {
+
+// Every GPU that loads the library holds this array until the process exits.
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;  // 32 MiB
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+// Device address of g_static_scratch, per device.  In host code the symbol is
+// only a host-side stand-in, never a device address.
+std::map<int, void*> g_static_scratch_addr;
+
+sgemm_status_t static_scratch_address(int dev, void** out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  auto it = g_static_scratch_addr.find(dev);
+  if (it == g_static_scratch_addr.end()) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return SGEMM_ERR_LAUNCH;
+    }
+    it = g_static_scratch_addr.emplace(dev, p).first;
+  }
+  *out = it->second;
+  return SGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" sgemm_status_t sgemm_streamk_static(int64_t M, int64_t N, int64_t K, const float* A,
+                                               int64_t lda, const float* B, int64_t ldb, float* C,
+                                               int64_t ldc, cudaStream_t stream) {
+  sgemm_status_t st = validate(M, N, K, A, lda, B, ldb, C, ldc);
+  if (st != SGEMM_OK) return st;
+  DeviceState* ds = nullptr;
+  int dev = 0;
+  st = device_state(&ds, &dev);
+  if (st != SGEMM_OK) return st;
+  if (M == 0 || N == 0) return SGEMM_OK;
+  if (K == 0) {
+    return gb300::launch_zero_fill(M, N, C, ldc, stream) == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+  }
+  if (!fast_path_ok(A, lda, B, ldb, C, ldc)) return SGEMM_ERR_INVALID_VALUE;
+  Plan p;
+  if (!make_plan(SGEMM_VARIANT_STREAMK, M, N, K, *ds, &p)) return SGEMM_ERR_UNSUPPORTED;
+  if (p.workspace_bytes() > kStaticScratchBytes) return SGEMM_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  st = static_scratch_address(dev, &scratch);
+  if (st != SGEMM_OK) return st;
+  const TileShape ts = gb300::tile_shape(p.cfg);
+
+  CUtensorMap tmap_a, tmap_b;
+  std::memset(&tmap_a, 0, sizeof(tmap_a));
+  std::memset(&tmap_b, 0, sizeof(tmap_b));
+  const cuuint32_t estr[2] = {1, 1};
+  {
+    const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(M)};
+    const cuuint64_t strides[1] = {cuuint64_t(lda) * 4};
+    const cuuint32_t box[2] = {cuuint32_t(ts.bk), cuuint32_t(ts.a_box_rows)};
+    if (g_encode(&tmap_a, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(A), dims, strides,
+                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return SGEMM_ERR_LAUNCH;
+  }
+  {
+    const cuuint64_t dims[2] = {cuuint64_t(N), cuuint64_t(K)};
+    const cuuint64_t strides[1] = {cuuint64_t(ldb) * 4};
+    const cuuint32_t box[2] = {cuuint32_t(ts.bn), cuuint32_t(ts.bk)};
+    if (g_encode(&tmap_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(B), dims, strides,
+                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return SGEMM_ERR_LAUNCH;
+  }
+
+  // The array keeps whatever the previous call left: the arrival counters of
+  // this call's split tiles must start at zero.
+  if (p.sc.sk_tiles > 0 &&
+      cudaMemsetAsync(scratch, 0, size_t(p.sc.sk_tiles) * sizeof(int32_t), stream) != cudaSuccess)
+    return SGEMM_ERR_LAUNCH;
+  gb300::GemmArgs args{};
+  args.M = int(M);
+  args.N = int(N);
+  args.K = int(K);
+  args.A = A;
+  args.lda = lda;
+  args.C = C;
+  args.ldc = ldc;
+  args.counters = static_cast<int32_t*>(scratch);
+  args.partials = reinterpret_cast<float*>(static_cast<char*>(scratch) + kCounterBytes);
+  args.status = ds->status;
+  args.wait_limit_ns = kDefaultWaitLimitNs;
+  return gb300::launch_tile_kernel(p.cfg, tmap_a, tmap_b, args, p.sc, p.grid, stream) == cudaSuccess
+             ? SGEMM_OK
+             : SGEMM_ERR_LAUNCH;
+}

@@ -122,6 +122,38 @@ const char *sgemm_variant_name(int variant);
  */
 sgemm_status_t sgemm_debug_expire_wait(uint64_t limit_ns, cudaStream_t stream);
 
+/*
+ * C = A * B with the Stream-K schedule (SGEMM_VARIANT_STREAMK), allocating
+ * nothing.  The pages have no counterpart: this entry point exists for
+ * callers that cannot let a library call cudaMalloc -- code that runs while
+ * its stream is being captured, code that must never wait on the whole
+ * device (cudaMalloc and cudaFree may synchronise it), and code that hands
+ * out a fixed memory budget before any work starts.
+ *
+ * Arguments, layout and ownership are those of sgemm().  The Stream-K
+ * scratch (arrival counters and partial sums of split tiles) lives in one
+ * fixed 32 MiB array in the library's device image, which every GPU that
+ * loads the library holds until the process exits.  No call allocates or
+ * frees memory, and no library routine that does is called.
+ *
+ * - The first call on a device looks up the array's device address (set-up,
+ *   once per device, with that device current); make that first call before
+ *   any stream capture begins.
+ * - Every call shares the one array: calls whose kernels overlap on the GPU
+ *   (for example on two streams) race and corrupt each other's results.
+ *   Order them on one stream or with events.
+ * - Each call zeroes the counters it uses (an asynchronous memset on
+ *   `stream`) and leaves the rest of the array as the previous call left it.
+ * - Returns SGEMM_ERR_UNSUPPORTED, launching nothing, when the shape needs
+ *   more scratch than the array holds (sgemm_workspace_size(
+ *   SGEMM_VARIANT_STREAMK, M, N, K) > 32 MiB), and SGEMM_ERR_INVALID_VALUE
+ *   for operands the pipelined kernel cannot take (a pointer not 16-byte
+ *   aligned, or a row stride that is not a multiple of 4).
+ */
+sgemm_status_t sgemm_streamk_static(int64_t M, int64_t N, int64_t K, const float *A,
+                                    int64_t lda, const float *B, int64_t ldb, float *C,
+                                    int64_t ldc, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
