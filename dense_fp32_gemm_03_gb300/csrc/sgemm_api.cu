@@ -55,7 +55,7 @@ struct Workspace {
 // environment variables SGEMM_TILE_LARGE / SGEMM_TILE_SMALL (a configuration
 // id) override them, for tuning sweeps.
 int g_cfg_large = 0;
-int g_cfg_small = 1;
+int g_cfg_small = 3;
 
 int env_config(const char* name, int fallback) {
   const char* v = std::getenv(name);

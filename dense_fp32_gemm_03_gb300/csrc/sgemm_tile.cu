@@ -11,9 +11,8 @@
 //    straight into a STAGES-deep ring.  Each producer warp copies its own
 //    32-row slice of every A tile into a private staging ring laid out with
 //    the 64-byte swizzle, then rewrites it transposed (k-major, "Vectorized
-//    Memory Access ...", section 4) with every value stored twice side by
-//    side, so that one 128-bit shared load yields ready-made operand pairs
-//    (a, a) for the paired FMA.  This is the multi-stage copy pipeline of
+//    Memory Access ...", section 4) so that one 128-bit shared load yields
+//    four rows of A at one k.  This is the multi-stage copy pipeline of
 //    "Beyond Kernel 7", section "Kernel 8", with the bulk copy engine in
 //    place of per-thread cp.async; A never passes through the compute warps'
 //    registers or the L1 request path.  The producers give most of their
@@ -22,7 +21,11 @@
 //    patch of C ("Beyond Kernel 7", section "Kernel 10"), updated per k step
 //    as a register outer product ("2D Block Tiling ...", section 4) with
 //    fma.rn.f32x2: one instruction performs two FP32 FFMAs, each with its own
-//    single rounding, halving the issue slots the arithmetic takes.
+//    single rounding, halving the issue slots the arithmetic takes.  The A
+//    operand enters as the pair (a, a); building that pair in registers
+//    costs no instruction (measured: the broadcast folds into the FFMA2),
+//    so A is stored once and read with half the shared-memory traffic of a
+//    doubled layout.
 //  Producers and consumers meet only at per-stage mbarriers ("full": the
 //  stage holds data; "empty": every consumer warp is done with it), so the
 //  compute loop has no block-wide barrier.
@@ -71,7 +74,7 @@ struct TileCfg {
   static constexpr int S = STAGES;
   static constexpr int S2 = ASTAGES;
   static constexpr bool kDoubleBuffer = DB;
-  static constexpr int kAStride = 2 * BM;  // floats per k row of the doubled, transposed A tile
+  static constexpr int kAStride = BM;  // floats per k row of the transposed A tile
   static constexpr int kAStageFloats = BK * kAStride;
   static constexpr int kBStageFloats = BK * BN;
   static constexpr int kAStagingFloats = kRowsPerProducer * BK;  // one producer warp's slot
@@ -98,10 +101,10 @@ struct TileCfg {
 // The compiled tile configurations (index = TileConfig id).
 using Cfg0 = TileCfg<4, 2, 16, 4, 4, false, 1>;  // 128 x 256 tile, 8 + 4 warps, 8x16 patch
 using Cfg1 = TileCfg<4, 1, 16, 4, 4, false, 2>;  // 128 x 128 tile, 4 + 4 warps, 2 CTAs / SM
-using Cfg2 = TileCfg<4, 2, 16, 6, 4, false, 1>;  // Cfg0 with a deeper ring
+using Cfg2 = TileCfg<4, 2, 16, 4, 4, true, 1>;   // Cfg0 with fragment double buffering
 using Cfg3 = TileCfg<4, 2, 8, 4, 4, true, 1>;    // 128 x 128 tile, 8 + 4 warps, 8x8 patch
-using Cfg4 = TileCfg<4, 2, 16, 3, 3, false, 1>;  // Cfg0 with a shallower ring
-using Cfg5 = TileCfg<4, 1, 16, 3, 3, false, 2>;  // Cfg1 with a shallower ring
+using Cfg4 = TileCfg<4, 2, 16, 3, 3, true, 1>;   // Cfg2 with a shallower ring
+using Cfg5 = TileCfg<4, 2, 8, 4, 4, false, 1>;   // Cfg3 without double buffering
 
 template <class F>
 auto with_cfg(int id, F&& f) {
@@ -285,21 +288,21 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
                          &full[s]);
       }
       if (!dev::mbar_wait_abortable(&my_astage[s2], n2 & 1u, limit, s_abort)) fail(kWaitTileStage);
-      // Transpose and double this warp's 32 rows: staging [r][k] (64-byte
-      // swizzled rows: 16-byte chunk q of row r sits at q ^ ((r >> 1) & 3))
-      // -> ring [k][2m].
+      // Transpose this warp's 32 rows: staging [r][k] (64-byte swizzled rows:
+      // 16-byte chunk q of row r sits at q ^ ((r >> 1) & 3)) -> ring [k][m].
+      // Consecutive lanes write consecutive m: conflict-free 4-byte stores.
       {
         const int r = lane;                    // row within this warp's slice
         const int m = pw * T::kRowsPerProducer + r;  // row within the tile
         const float* src = my_staging + s2 * T::kAStagingFloats + r * T::BK;
-        float* d = sA + s * T::kAStageFloats + 2 * m;
+        float* d = sA + s * T::kAStageFloats + m;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const float4 v = *reinterpret_cast<const float4*>(src + (q ^ ((r >> 1) & 3)) * 4);
-          *reinterpret_cast<float2*>(d + (4 * q + 0) * T::kAStride) = make_float2(v.x, v.x);
-          *reinterpret_cast<float2*>(d + (4 * q + 1) * T::kAStride) = make_float2(v.y, v.y);
-          *reinterpret_cast<float2*>(d + (4 * q + 2) * T::kAStride) = make_float2(v.z, v.z);
-          *reinterpret_cast<float2*>(d + (4 * q + 3) * T::kAStride) = make_float2(v.w, v.w);
+          d[(4 * q + 0) * T::kAStride] = v.x;
+          d[(4 * q + 1) * T::kAStride] = v.y;
+          d[(4 * q + 2) * T::kAStride] = v.z;
+          d[(4 * q + 3) * T::kAStride] = v.w;
         }
       }
       __syncwarp();
@@ -331,7 +334,7 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(T::kRegsConsumer));
   const int tr = lane / T::kTC, tc = lane % T::kTC;
   const int wm = warp % T::kWarpsM, wn = warp / T::kWarpsM;
-  const int a_frag = 2 * wm * T::kWarpM + 4 * tr;  // + 16 g + kAStride kk
+  const int a_frag = wm * T::kWarpM + 4 * tr;  // + 16 g + kAStride kk
   const int b_frag = wn * T::kWarpN + 4 * tc;      // + 32 h + BN kk
   const int M = args.M, N = args.N;
 
@@ -357,12 +360,12 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
       const float* a_buf = sA + s * T::kAStageFloats + a_frag;
       const float* b_buf = sB + s * T::kBStageFloats + b_frag;
       struct Frag {
-        float4 a[T::kTM / 2];  // (a[m], a[m], a[m+1], a[m+1]) for the thread's row pairs
+        float4 a[T::kTM / 4];  // A at rows m .. m+3 of each of the thread's row quads
         float4 b[T::kTN / 4];  // four consecutive B values per column quad
       };
       auto load_frag = [&](Frag& f, int kk) {
 #pragma unroll
-        for (int g = 0; g < T::kTM / 2; ++g)
+        for (int g = 0; g < T::kTM / 4; ++g)
           f.a[g] = *reinterpret_cast<const float4*>(a_buf + kk * T::kAStride + 16 * g);
 #pragma unroll
         for (int h = 0; h < T::kTN / 4; ++h)
@@ -371,16 +374,21 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
       // B-major order: consecutive FFMA2s share one B pair and walk the rows,
       // which measured markedly faster than row-major orders on sm_103a.
       auto fma_frag = [&](const Frag& f) {
+        float2 ap[T::kTM];  // (a, a) for each of the thread's rows
+#pragma unroll
+        for (int g = 0; g < T::kTM / 4; ++g) {
+          ap[4 * g + 0] = make_float2(f.a[g].x, f.a[g].x);
+          ap[4 * g + 1] = make_float2(f.a[g].y, f.a[g].y);
+          ap[4 * g + 2] = make_float2(f.a[g].z, f.a[g].z);
+          ap[4 * g + 3] = make_float2(f.a[g].w, f.a[g].w);
+        }
 #pragma unroll
         for (int h = 0; h < T::kTN / 4; ++h) {
 #pragma unroll
           for (int p = 0; p < 2; ++p) {
             const float2 bq = p ? make_float2(f.b[h].z, f.b[h].w) : make_float2(f.b[h].x, f.b[h].y);
 #pragma unroll
-            for (int g = 0; g < T::kTM / 2; ++g) {
-              dev::ffma2(acc[2 * g][2 * h + p], make_float2(f.a[g].x, f.a[g].y), bq);
-              dev::ffma2(acc[2 * g + 1][2 * h + p], make_float2(f.a[g].z, f.a[g].w), bq);
-            }
+            for (int r = 0; r < T::kTM; ++r) dev::ffma2(acc[r][2 * h + p], ap[r], bq);
           }
         }
       };
@@ -408,7 +416,7 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
     // Thread value j is the float4 of patch row r = j / Q, column quad h = j % Q.
     constexpr int Q = T::kTN / 4;
     auto out_row = [&](int r) {
-      return m0 + wm * T::kWarpM + (r >> 1) * (2 * T::kTR) + 2 * tr + (r & 1);
+      return m0 + wm * T::kWarpM + (r >> 2) * (4 * T::kTR) + 4 * tr + (r & 3);
     };
     auto out_col = [&](int h) { return n0 + wn * T::kWarpN + h * (4 * T::kTC) + 4 * tc; };
     auto value = [&](int j) {
