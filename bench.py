@@ -42,7 +42,7 @@ FFMA_PER_CLK_PER_SM = 128  # FP32 lanes per SM: one FFMA each per clock
 def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--steps", type=int, default=500)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="square_4096_uniform")
@@ -175,15 +175,28 @@ def ffma_peak_tflops(sms: int, mhz: float) -> float:
     return sms * FFMA_PER_CLK_PER_SM * 2 * mhz * 1e6 / 1e12
 
 
-def measured_traffic():
-    """DRAM bytes per launch of the tile kernel at 4096^3, from the committed ncu summary."""
-    path = os.path.join(ROOT, "profiles", "tile_kernel_4096.json")
+def kernel_source_digest() -> str:
+    """SHA-256 of the tile kernel's source: profile counters apply only to this exact kernel."""
+    import hashlib
+    path = os.path.join(ROOT, "dense_fp32_gemm_03_gb300", "csrc", "sgemm_tile.cu")
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes per launch of the tile kernel on ``workload`` from the committed ncu
+    summary, or None when there is none or the kernel source changed since it was taken."""
+    import re
+    path = os.path.join(ROOT, "profiles", f"tile_kernel_{workload}.md")
     try:
-        with open(path) as f:
-            d = json.load(f)
-        return d.get("dram_bytes_per_launch"), d.get("kernel_build")
-    except (OSError, ValueError):
-        return None, None
+        text = open(path).read()
+    except OSError:
+        return None
+    digest = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
+    traffic = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not digest or not traffic or digest.group(1) != kernel_source_digest():
+        return None
+    return float(traffic.group(1))
 
 
 def cpu_baseline(w, A, B, seconds: float):
@@ -324,7 +337,7 @@ def run_ours(args):
     kernel_tflops = w.flops / (statistics.mean(times) * 1e-3) / 1e12
     peak_max = ffma_peak_tflops(sms, clock["sm_max_mhz"] or 2070.0)
     peak_run = ffma_peak_tflops(sms, clock["sm_mhz"]) if clock["sm_mhz"] else None
-    traffic, _ = measured_traffic()
+    traffic = measured_traffic(w.name)
 
     # End to end through the C ABI with pinned host buffers.
     A_pin = A_h.pin_memory()

@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -211,34 +212,52 @@ bool make_plan(int variant, int64_t M, int64_t N, int64_t K, const DeviceState& 
   return true;
 }
 
-// The selector: aligned operands take a pipelined variant, the rest the guarded kernel.
+// Estimated duration (microseconds) of a planned fast variant on this device.
+// The model was fitted to measured GB300 timings of the compiled
+// configurations: every CTA slot streams its k-tiles at a fixed efficiency
+// of the FFMA peak (86% with 8x16 patches, 80% with 8x8), plus a fixed cost
+// per launch and, when tiles are split, the time the last CTA of a tile
+// spends reading the partial sums back.
+double plan_cost_us(const Plan& p, const DeviceState& ds) {
+  const TileShape ts = gb300::tile_shape(p.cfg);
+  const int cps = ds.ctas_per_sm[p.cfg] > 0 ? ds.ctas_per_sm[p.cfg] : 1;
+  const double flop_per_us_per_sm = 128.0 * 2.0 * 2070.0;  // FFMA lanes x 2 x max clock (MHz)
+  const double eff = ts.patch_n == 16 ? 0.86 : 0.80;
+  const double ktile_us = double(ts.bm) * ts.bn * ts.bk * 2.0 * cps / (flop_per_us_per_sm * eff);
+  const int64_t resident = int64_t(ds.sms) * cps;
+  const double ipt = p.sc.iters_per_tile;
+  if (p.sc.sk_tiles == 0 && p.sc.dp_tiles == int64_t(p.sc.tiles_m) * p.sc.tiles_n &&
+      p.grid == p.sc.dp_tiles) {
+    // One tile per CTA: whole waves of CTA slots.
+    const int64_t waves = (int64_t(p.sc.dp_tiles) + resident - 1) / resident;
+    return 8.0 + double(waves) * ipt * ktile_us;
+  }
+  const double dp_waves = double(p.sc.dp_tiles) / double(resident);
+  double iters = dp_waves * ipt;
+  double fixup = 0.0;
+  if (p.sc.sk_tiles > 0) {
+    iters += double(p.sc.sk_base + (p.sc.sk_extra ? 1 : 0));
+    // The last CTA of a split tile reads every segment's partial tile back.
+    const double tile_kb = double(ts.bm) * ts.bn * 4.0 / 1024.0;
+    const double segments = std::ceil(double(p.sc.sk_ctas) / double(p.sc.sk_tiles)) + 1.0;
+    fixup = 0.015 * tile_kb * segments;
+  }
+  return 10.0 + iters * ktile_us + fixup;
+}
+
+// The selector: aligned operands take the pipelined variant with the lowest
+// estimated time; the rest take the guarded kernel.
 int select_variant(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
                    int64_t ldb, const float* C, int64_t ldc, const DeviceState& ds) {
   if (!fast_path_ok(A, lda, B, ldb, C, ldc)) return SGEMM_VARIANT_GUARDED;
-  // Estimated time of each candidate in units of one large-tile k-iteration on
-  // one SM: the busiest SM's share of the k-tiles, plus a charge per split.
   int best = SGEMM_VARIANT_STREAMK;
   double best_cost = 1e300;
-  const int candidates[4] = {SGEMM_VARIANT_STREAMK, SGEMM_VARIANT_TILED,
-                             SGEMM_VARIANT_STREAMK_SMALL, SGEMM_VARIANT_TILED_SMALL};
+  const int candidates[4] = {SGEMM_VARIANT_STREAMK, SGEMM_VARIANT_STREAMK_SMALL,
+                             SGEMM_VARIANT_TILED, SGEMM_VARIANT_TILED_SMALL};
   for (int v : candidates) {
     Plan p;
     if (!make_plan(v, M, N, K, ds, &p)) continue;
-    const TileShape ts = gb300::tile_shape(p.cfg);
-    const double tile_work = double(ts.bm) * ts.bn / (128.0 * 256.0);  // relative to a large tile
-    const int cps = ds.ctas_per_sm[p.cfg];
-    const double ipt = p.sc.iters_per_tile;
-    double cost;
-    if (p.sc.sk_tiles == 0) {
-      const int64_t resident = int64_t(ds.sms) * cps;
-      const int64_t tiles = int64_t(p.sc.tiles_m) * p.sc.tiles_n;
-      const int64_t waves = (tiles + resident - 1) / resident;
-      cost = double(waves) * ipt * tile_work * cps;
-    } else {
-      const double per_cta = double(p.sc.sk_base + (p.sc.sk_extra ? 1 : 0));
-      const double dp_waves = p.sc.dp_tiles / double(int64_t(ds.sms) * cps);
-      cost = (dp_waves * ipt + per_cta) * tile_work * cps + 2.0 * tile_work;  // fixup ~ 2 k-tiles
-    }
+    const double cost = plan_cost_us(p, ds);
     if (cost < best_cost * 0.999) {
       best_cost = cost;
       best = v;

@@ -57,6 +57,8 @@ struct TileShape {
   int bm, bn, bk, threads, stages;
   size_t smem_bytes;
   int a_box_rows;  // rows of A per TMA copy (one producer warp's slice)
+  int patch_n;     // outputs per thread along N (16 or 8)
+  int ctas_per_sm; // CTAs the configuration is built to co-reside per SM
 };
 
 TileShape tile_shape(TileConfig cfg);

@@ -472,31 +472,33 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
     const bool last = *s_last != 0;
     dev::named_barrier(1, T::kConsumers);  // s_last may be rewritten by the next split tile
     if (last) {
+      // Every partial, this CTA's included, is in the workspace: sum them in
+      // CTA order with all of a slot's loads in flight at once.
       __threadfence();
+      const float4* base = reinterpret_cast<const float4*>(args.partials) + tid;
+      const int64_t slot_vec = tile_floats / 4;
+      float4 sum[T::kOutVec];
+      {
+        const float4* src = base + (u.t_sk + c_first) * slot_vec;
 #pragma unroll
-      for (int j = 0; j < T::kOutVec; ++j) {
-        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 1
-        for (int cc = c_first; cc <= c_last; ++cc) {
-          float4 v;
-          if (cc == cta) {
-            v = value(j);
-          } else {
-            const float4* src =
-                reinterpret_cast<const float4*>(args.partials + (u.t_sk + cc) * tile_floats);
-            v = __ldcg(src + j * T::kConsumers + tid);
-          }
-          if (cc == c_first) {
-            sum = v;
-          } else {
-            sum.x += v.x;
-            sum.y += v.y;
-            sum.z += v.z;
-            sum.w += v.w;
-          }
-        }
-        store_c(j, sum);
+        for (int j = 0; j < T::kOutVec; ++j) sum[j] = __ldcg(src + j * T::kConsumers);
       }
+#pragma unroll 1
+      for (int cc = c_first + 1; cc <= c_last; ++cc) {
+        const float4* src = base + (u.t_sk + cc) * slot_vec;
+        float4 v[T::kOutVec];
+#pragma unroll
+        for (int j = 0; j < T::kOutVec; ++j) v[j] = __ldcg(src + j * T::kConsumers);
+#pragma unroll
+        for (int j = 0; j < T::kOutVec; ++j) {
+          sum[j].x += v[j].x;
+          sum[j].y += v[j].y;
+          sum[j].z += v[j].z;
+          sum[j].w += v[j].w;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < T::kOutVec; ++j) store_c(j, sum[j]);
       if (tid == 0) args.counters[u.t_sk] = 0;
     }
   }
@@ -516,7 +518,8 @@ int prepare() {
 
 template <class T>
 TileShape shape_of() {
-  return TileShape{T::BM, T::BN, T::BK, T::NT, T::S, T::kSmem, T::kRowsPerProducer};
+  return TileShape{T::BM, T::BN, T::BK, T::NT, T::S, T::kSmem, T::kRowsPerProducer, T::kTN,
+                   T::kCtasPerSm};
 }
 
 }  // namespace
