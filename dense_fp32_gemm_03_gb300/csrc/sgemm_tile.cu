@@ -48,7 +48,8 @@ namespace {
 
 constexpr uint32_t kStatusTimeout = 3;  // SGEMM_ERR_TIMEOUT
 
-template <int WARPS_M, int WARPS_N, int TN, int STAGES, int ASTAGES, bool DB, int CTAS>
+template <int WARPS_M, int WARPS_N, int TN, int STAGES, int ASTAGES, bool DB, int CTAS,
+          int PRODUCER_REGS = 56>
 struct TileCfg {
   static constexpr int kTR = 4, kTC = 8;    // lane grid of a consumer warp: rows x columns
   static constexpr int kTM = 8, kTN = TN;   // outputs per thread
@@ -64,7 +65,7 @@ struct TileCfg {
   // Registers: the launch gives every thread R0; the producer warpgroup then
   // hands registers to the consumer warpgroups (setmaxnreg), keeping the total.
   static constexpr int kRegsLaunch = (65536 / (CTAS * NT)) / 8 * 8;
-  static constexpr int kRegsProducer = 56;
+  static constexpr int kRegsProducer = PRODUCER_REGS;
   static constexpr int kRegsConsumer =
       ((NT * kRegsLaunch - kProducers * kRegsProducer) / kConsumers) / 8 * 8;
   static constexpr int BM = WARPS_M * kWarpM;
@@ -99,12 +100,12 @@ struct TileCfg {
 };
 
 // The compiled tile configurations (index = TileConfig id).
-using Cfg0 = TileCfg<4, 2, 16, 4, 4, false, 1>;  // 128 x 256 tile, 8 + 4 warps, 8x16 patch
-using Cfg1 = TileCfg<4, 1, 16, 4, 4, false, 2>;  // 128 x 128 tile, 4 + 4 warps, 2 CTAs / SM
-using Cfg2 = TileCfg<4, 2, 16, 4, 4, true, 1>;   // Cfg0 with fragment double buffering
-using Cfg3 = TileCfg<4, 2, 8, 4, 4, true, 1>;    // 128 x 128 tile, 8 + 4 warps, 8x8 patch
-using Cfg4 = TileCfg<4, 2, 16, 3, 3, true, 1>;   // Cfg2 with a shallower ring
-using Cfg5 = TileCfg<4, 2, 8, 4, 4, false, 1>;   // Cfg3 without double buffering
+using Cfg0 = TileCfg<4, 2, 16, 4, 4, false, 1>;      // 128 x 256 tile, 8 + 4 warps, 8x16 patch
+using Cfg1 = TileCfg<4, 1, 16, 4, 4, false, 2, 40>;  // 128 x 128 tile, 4 + 4 warps, 2 CTAs / SM
+using Cfg2 = TileCfg<4, 2, 16, 4, 4, true, 1>;       // Cfg0 with fragment double buffering
+using Cfg3 = TileCfg<4, 2, 8, 4, 4, true, 1>;        // 128 x 128 tile, 8 + 4 warps, 8x8 patch
+using Cfg4 = TileCfg<4, 1, 16, 3, 3, false, 2, 40>;  // Cfg1 with a shallower ring
+using Cfg5 = TileCfg<4, 1, 16, 6, 2, false, 2, 40>;  // Cfg1 with a deeper B / A ring
 
 template <class F>
 auto with_cfg(int id, F&& f) {
