@@ -22,7 +22,8 @@ VARIANTS = {"guarded": GUARDED, "tiled": TILED, "streamk": STREAMK,
 # Every entry point include/sgemm.h declares.
 EXPORTS = ("sgemm", "sgemm_variant", "sgemm_select_variant", "sgemm_workspace_size",
            "sgemm_query_device_status", "sgemm_release_workspaces", "sgemm_status_string",
-           "sgemm_variant_name", "sgemm_debug_expire_wait", "sgemm_streamk_static")
+           "sgemm_variant_name", "sgemm_debug_expire_wait", "sgemm_streamk_static",
+           "sgemm_tf32")
 
 
 class SgemmError(RuntimeError):
@@ -74,6 +75,8 @@ def load(path: str | None = None):
         lib.sgemm_debug_expire_wait.restype = st
         lib.sgemm_streamk_static.argtypes = gemm_args
         lib.sgemm_streamk_static.restype = st
+        lib.sgemm_tf32.argtypes = gemm_args
+        lib.sgemm_tf32.restype = st
         _lib = lib
         return lib
 
@@ -104,7 +107,8 @@ def _check_operand(t, name):
         raise ValueError(f"{name} must be a 2-D float32 CUDA tensor, got {t.dtype} {tuple(t.shape)} on {t.device}")
     if t.shape[1] > 1 and t.stride(1) != 1:
         raise ValueError(f"{name} must be row-major (unit column stride)")
-    return max(t.stride(0), t.shape[1], 1) if t.shape[0] > 1 else max(t.shape[1], 1)
+    # Row stride in elements; for a single row it only has to cover the row.
+    return max(t.stride(0), t.shape[1], 1)
 
 
 def _stream_handle(device, stream=None):
@@ -139,6 +143,26 @@ def sgemm(A, B, out=None, variant: int = AUTO, stream=None):
                        _stream_handle(A.device, stream), variant)
     if st != OK:
         raise SgemmError(st, "sgemm")
+    return out
+
+
+def sgemm_tf32(A, B, out=None, stream=None):
+    """Opt-in TF32 tensor-core mode (not FP32 arithmetic): C = A @ B with TF32 products."""
+    import torch
+    lda = _check_operand(A, "A")
+    ldb = _check_operand(B, "B")
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: {tuple(A.shape)} @ {tuple(B.shape)}")
+    if out is None:
+        out = torch.empty((M, N), device=A.device, dtype=torch.float32)
+    ldc = _check_operand(out, "out")
+    with torch.cuda.device(A.device):
+        st = load().sgemm_tf32(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc,
+                               _stream_handle(A.device, stream))
+    if st != OK:
+        raise SgemmError(st, "sgemm_tf32")
     return out
 
 

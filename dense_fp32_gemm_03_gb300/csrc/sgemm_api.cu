@@ -44,6 +44,7 @@ struct DeviceState {
   sgemm_status_t init_status = SGEMM_OK;
   int sms = 0;
   int ctas_per_sm[gb300::kTileConfigs] = {};
+  int tf32_ctas_per_sm = 0;
   uint32_t* status = nullptr;
 };
 
@@ -92,6 +93,8 @@ sgemm_status_t device_state(DeviceState** out, int* dev_out) {
         st.ctas_per_sm[c] = gb300::tile_kernel_prepare(TileConfig(c));
         if (st.ctas_per_sm[c] <= 0) st.init_status = SGEMM_ERR_LAUNCH;
       }
+      st.tf32_ctas_per_sm = gb300::tf32_prepare();
+      if (st.tf32_ctas_per_sm <= 0) st.init_status = SGEMM_ERR_LAUNCH;
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) {
         st.init_status = SGEMM_ERR_LAUNCH;
@@ -266,8 +269,7 @@ int select_variant(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
   return best;
 }
 
-sgemm_status_t get_workspace(int dev, cudaStream_t stream, const Plan& p, void** out) {
-  const size_t need = p.workspace_bytes();
+sgemm_status_t get_workspace_bytes(int dev, cudaStream_t stream, size_t need, void** out) {
   *out = nullptr;
   if (need == 0) return SGEMM_OK;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -293,6 +295,10 @@ sgemm_status_t get_workspace(int dev, cudaStream_t stream, const Plan& p, void**
   }
   *out = ws.ptr;
   return SGEMM_OK;
+}
+
+sgemm_status_t get_workspace(int dev, cudaStream_t stream, const Plan& p, void** out) {
+  return get_workspace_bytes(dev, stream, p.workspace_bytes(), out);
 }
 
 sgemm_status_t run(int variant, int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
@@ -397,6 +403,61 @@ size_t sgemm_workspace_size(int variant, int64_t M, int64_t N, int64_t K) {
   Plan p;
   if (!make_plan(variant, M, N, K, *ds, &p)) return 0;
   return p.workspace_bytes();
+}
+
+sgemm_status_t sgemm_tf32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+                          const float* B, int64_t ldb, float* C, int64_t ldc, cudaStream_t stream) {
+  sgemm_status_t st = validate(M, N, K, A, lda, B, ldb, C, ldc);
+  if (st != SGEMM_OK) return st;
+  DeviceState* ds = nullptr;
+  int dev = 0;
+  st = device_state(&ds, &dev);
+  if (st != SGEMM_OK) return st;
+  if (M == 0 || N == 0) return SGEMM_OK;
+  if (K == 0) {
+    return gb300::launch_zero_fill(M, N, C, ldc, stream) == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+  }
+  // A goes to the tensor cores by TMA and C is stored 128 bits at a time.
+  if (!aligned16(A) || !aligned16(C) || lda % 4 != 0 || ldc % 4 != 0) return SGEMM_ERR_INVALID_VALUE;
+  const int64_t tiles = ((M + gb300::tf32_tile_m() - 1) / gb300::tf32_tile_m()) *
+                        ((N + gb300::tf32_tile_n() - 1) / gb300::tf32_tile_n());
+  if (tiles > kInt32Max) return SGEMM_ERR_UNSUPPORTED;
+  // B^T (N x K, rows padded to a multiple of 4 floats) lives in the workspace,
+  // after the counter region the Stream-K schedule relies on.
+  const int64_t ldbt = (K + 3) / 4 * 4;
+  void* ws = nullptr;
+  st = get_workspace_bytes(dev, stream, kCounterBytes + size_t(N) * size_t(ldbt) * 4, &ws);
+  if (st != SGEMM_OK) return st;
+  float* Bt = reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes);
+  if (gb300::launch_transpose(B, ldb, Bt, ldbt, int(K), int(N), stream) != cudaSuccess)
+    return SGEMM_ERR_LAUNCH;
+
+  CUtensorMap tmap_a, tmap_bt;
+  std::memset(&tmap_a, 0, sizeof(tmap_a));
+  std::memset(&tmap_bt, 0, sizeof(tmap_bt));
+  const cuuint32_t estr[2] = {1, 1};
+  {
+    const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(M)};
+    const cuuint64_t strides[1] = {cuuint64_t(lda) * 4};
+    const cuuint32_t box[2] = {cuuint32_t(gb300::tf32_tile_k()), cuuint32_t(gb300::tf32_tile_m())};
+    if (g_encode(&tmap_a, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(A), dims, strides,
+                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return SGEMM_ERR_LAUNCH;
+  }
+  {
+    const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(N)};
+    const cuuint64_t strides[1] = {cuuint64_t(ldbt) * 4};
+    const cuuint32_t box[2] = {cuuint32_t(gb300::tf32_tile_k()), cuuint32_t(gb300::tf32_tile_n())};
+    if (g_encode(&tmap_bt, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, Bt, dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return SGEMM_ERR_LAUNCH;
+  }
+  return gb300::launch_tf32_kernel(tmap_a, tmap_bt, int(M), int(N), int(K), C, ldc, kGroupM,
+                                   ds->status, kDefaultWaitLimitNs, stream) == cudaSuccess
+             ? SGEMM_OK
+             : SGEMM_ERR_LAUNCH;
 }
 
 sgemm_status_t sgemm_query_device_status(cudaStream_t stream, uint32_t* detail) {

@@ -73,6 +73,21 @@ cudaError_t launch_tile_kernel(TileConfig cfg, const CUtensorMap& tmap_a, const 
                                const GemmArgs& args, const Sched& sched, int grid,
                                cudaStream_t stream);
 
+// TF32 tensor-core mode (sgemm_tf32.cu): 128 x 256 output tiles, 32-deep k slices.
+size_t tf32_smem_bytes();
+int tf32_tile_m();
+int tf32_tile_n();
+int tf32_tile_k();
+int tf32_prepare();  // resident CTAs per SM, or < 0 on error
+// Bt (N x K, row stride ldbt, K contiguous) = B^T.
+cudaError_t launch_transpose(const float* B, int64_t ldb, float* Bt, int64_t ldbt, int K, int N,
+                             cudaStream_t stream);
+// tmap_a: A (K fastest), box {32, 128}; tmap_bt: Bt (K fastest), box {32, 256}; both with the
+// 128-byte swizzle.
+cudaError_t launch_tf32_kernel(const CUtensorMap& tmap_a, const CUtensorMap& tmap_bt, int M, int N,
+                               int K, float* C, int64_t ldc, int group_m, uint32_t* status,
+                               uint64_t limit, cudaStream_t stream);
+
 cudaError_t launch_guarded_kernel(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
                                   const float* B, int64_t ldb, float* C, int64_t ldc,
                                   cudaStream_t stream);

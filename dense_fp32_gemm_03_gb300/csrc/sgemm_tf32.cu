@@ -1,0 +1,271 @@
+// sgemm_tf32.cu -- opt-in TF32 tensor-core GEMM for sm_103a (tcgen05).
+//
+// C = A * B with the products formed by the 5th-generation tensor cores in
+// TF32 (inputs keep FP32's exponent and 10 fraction bits) and accumulated in
+// FP32.  This is a separate mode with its own, looser tolerance: TF32 is the
+// different-numerics tensor path the pages name ("Beyond Kernel 7", section
+// "The operation: GEMM and the precision of the comparison"; "cuSgemm",
+// Kernel 7 uses mma.sync m16n8k4 TF32 on sm_120).  It never stands in for the
+// FP32 FFMA path.
+//
+// Structure (one output tile of 128 x 256 per CTA):
+//  * B is first rewritten K-major (transpose_kernel) so that both operands
+//    reach shared memory by TMA already in the canonical K-major layout with
+//    the 128-byte swizzle that tcgen05.mma reads through its shared-memory
+//    descriptors.
+//  * warp 0 (one lane) streams 32-deep k-slices of A (128 x 32) and B^T
+//    (256 x 32) into a 4-stage ring (full / empty mbarriers);
+//  * warp 1 allocates 256 TMEM columns and one lane issues
+//    tcgen05.mma.cta_group::1.kind::tf32 (M = 128, N = 256, K = 8, four per
+//    k-slice), releasing each stage with tcgen05.commit;
+//  * warps 2-5 wait for the accumulator, read it with tcgen05.ld (each warp
+//    its 32-lane quarter of TMEM, i.e. 32 rows of C) and store C.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "sgemm_device.cuh"
+#include "sgemm_internal.h"
+
+namespace gb300 {
+namespace {
+
+constexpr int kTfBM = 128, kTfBN = 256, kTfBK = 32, kTfStages = 4, kTfThreads = 192;
+constexpr uint32_t kTfAStageBytes = kTfBM * kTfBK * 4;  // 16 KB
+constexpr uint32_t kTfBStageBytes = kTfBN * kTfBK * 4;  // 32 KB
+constexpr uint32_t kTfTmemCols = 256;                   // 128 lanes x 256 FP32 columns
+constexpr size_t kTfSmem = 1024 /* alignment slack */ + kTfStages * size_t(kTfAStageBytes + kTfBStageBytes) +
+                           (2 * kTfStages + 1) * 8 + 16;
+constexpr uint32_t kStatusTimeout = 3;
+
+// Instruction descriptor of tcgen05.mma kind::tf32: FP32 accumulator, TF32 A
+// and B, both K-major, M = 128, N = 256.
+constexpr uint32_t kTfIdesc = (1u << 4)                 // D format: F32
+                              | (2u << 7)               // A format: TF32
+                              | (2u << 10)              // B format: TF32
+                              | (0u << 15) | (0u << 16) // A, B K-major
+                              | (uint32_t(kTfBN >> 3) << 17) | (uint32_t(kTfBM >> 4) << 24);
+
+// Shared-memory matrix descriptor for a K-major operand stored as rows of 128
+// bytes with the 128-byte swizzle: 8-row core groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= uint64_t((smem_addr & 0x3FFFFu) >> 4);  // start address
+  d |= uint64_t(16 >> 4) << 16;                // leading byte offset (unused when swizzled)
+  d |= uint64_t(1024 >> 4) << 32;              // stride byte offset between 8-row groups
+  d |= uint64_t(1) << 46;                      // descriptor version for sm_100 family
+  d |= uint64_t(2) << 61;                      // layout: 128-byte swizzle
+  return d;
+}
+
+__device__ __forceinline__ void tc_mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(kTfIdesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives on `bar` once every tcgen05 operation this thread issued so far completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   dev::smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kTfThreads, 1)
+    tf32_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_bt,
+                int M, int N, int K, float* __restrict__ C, int64_t ldc, int tiles_m, int tiles_n,
+                int group_m, uint32_t* status, uint64_t limit) {
+  extern __shared__ unsigned char smem_raw[];
+  // Stages must sit on 1024-byte boundaries (the 128-byte swizzle period).
+  const uint32_t raw = dev::smem_addr(smem_raw);
+  unsigned char* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  unsigned char* sA = smem;
+  unsigned char* sB = smem + kTfStages * kTfAStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kTfStages * kTfBStageBytes);
+  uint64_t* empty = full + kTfStages;
+  uint64_t* accum = empty + kTfStages;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(accum + 1);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(accum + 1) + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Grouped raster over tiles, as the FFMA kernel does.
+  const int tile = blockIdx.x;
+  const int per_group = group_m * tiles_n;
+  const int g = tile / per_group;
+  const int first = g * group_m;
+  const int rows = min(tiles_m - first, group_m);
+  const int m0 = (first + (tile - g * per_group) % rows) * kTfBM;
+  const int n0 = ((tile - g * per_group) / rows) * kTfBN;
+  const int num_k = (K + kTfBK - 1) / kTfBK;
+
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     dev::smem_addr(const_cast<uint32_t*>(tmem_slot))),
+                 "r"(kTfTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTfStages; ++s) {
+      dev::mbar_init(&full[s], 1);
+      dev::mbar_init(&empty[s], 1);
+    }
+    dev::mbar_init(accum, 1);
+    *s_abort = 0;
+    dev::mbar_init_fence();
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_slot;
+
+  auto fail = [&]() {
+    if (!*s_abort) {
+      *s_abort = 1;
+      dev::record_status(status, kStatusTimeout, kWaitTileStage);
+    }
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- TMA producer
+      dev::tma_prefetch_desc(&tmap_a);
+      dev::tma_prefetch_desc(&tmap_bt);
+      for (int kt = 0; kt < num_k; ++kt) {
+        const int s = kt % kTfStages, n = kt / kTfStages;
+        if (n > 0 && !dev::mbar_wait_abortable(&empty[s], (n - 1) & 1u, limit, s_abort)) fail();
+        if (*s_abort) break;
+        dev::mbar_arrive_expect_tx(&full[s], kTfAStageBytes + kTfBStageBytes);
+        dev::tma_load_2d(sA + s * kTfAStageBytes, &tmap_a, kt * kTfBK, m0, &full[s]);
+        dev::tma_load_2d(sB + s * kTfBStageBytes, &tmap_bt, kt * kTfBK, n0, &full[s]);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer
+      for (int kt = 0; kt < num_k; ++kt) {
+        const int s = kt % kTfStages;
+        if (!dev::mbar_wait_abortable(&full[s], (kt / kTfStages) & 1u, limit, s_abort)) {
+          fail();
+          break;
+        }
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint64_t a_desc = sw128_kmajor_desc(dev::smem_addr(sA + s * kTfAStageBytes));
+        const uint64_t b_desc = sw128_kmajor_desc(dev::smem_addr(sB + s * kTfBStageBytes));
+#pragma unroll
+        for (int k = 0; k < kTfBK / 8; ++k)  // K = 8 TF32 = 32 bytes per instruction
+          tc_mma_tf32(tmem, a_desc + 2 * k, b_desc + 2 * k, (kt | k) != 0 ? 1u : 0u);
+        tc_commit(&empty[s]);  // the stage is free once these MMAs have read it
+      }
+      tc_commit(accum);  // the accumulator is final once every MMA completed
+    }
+  } else {
+    // ---- epilogue: warps 2..5 own TMEM lane quarters (warp % 4)
+    const int q = warp & 3;
+    if (!dev::mbar_wait_abortable(accum, 0u, limit, s_abort)) fail();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const int row = m0 + 32 * q + lane;
+#pragma unroll 1
+    for (int c = 0; c < kTfBN; c += 32) {
+      uint32_t r[32];
+      tc_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(c), r);
+      if (row < M && !*s_abort) {
+        float* dst = C + int64_t(row) * ldc + n0 + c;
+        if (n0 + c + 32 <= N) {
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            reinterpret_cast<float4*>(dst)[v] =
+                make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                            __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+        } else {
+#pragma unroll
+          for (int v = 0; v < 32; ++v)
+            if (n0 + c + v < N) dst[v] = __uint_as_float(r[v]);
+        }
+      }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  }
+  __syncthreads();
+  if (warp == 1) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTfTmemCols)
+                 : "memory");
+  }
+}
+
+// Bt[n][k] = B[k][n] through 32 x 33 shared tiles (coalesced on both sides).
+__global__ void __launch_bounds__(256)
+    transpose_kernel(const float* __restrict__ B, int64_t ldb, float* __restrict__ Bt,
+                     int64_t ldbt, int K, int N) {
+  __shared__ float tile[32][33];
+  const int64_t n0 = int64_t(blockIdx.x) * 32;
+  const int64_t k_tiles = (int64_t(K) + 31) / 32;
+  for (int64_t ky = blockIdx.y; ky < k_tiles; ky += gridDim.y) {
+    const int64_t k0 = ky * 32;
+    for (int i = threadIdx.y; i < 32; i += 8) {
+      const int64_t k = k0 + i, n = n0 + threadIdx.x;
+      tile[i][threadIdx.x] = (k < K && n < N) ? B[k * ldb + n] : 0.f;
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += 8) {
+      const int64_t n = n0 + i, k = k0 + threadIdx.x;
+      if (n < N && k < K) Bt[n * ldbt + k] = tile[threadIdx.x][i];
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+size_t tf32_smem_bytes() { return kTfSmem; }
+int tf32_tile_m() { return kTfBM; }
+int tf32_tile_n() { return kTfBN; }
+int tf32_tile_k() { return kTfBK; }
+
+int tf32_prepare() {
+  if (cudaFuncSetAttribute(tf32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kTfSmem)) !=
+      cudaSuccess)
+    return -1;
+  int blocks = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, tf32_kernel, kTfThreads, kTfSmem) !=
+      cudaSuccess)
+    return -1;
+  return blocks;
+}
+
+cudaError_t launch_transpose(const float* B, int64_t ldb, float* Bt, int64_t ldbt, int K, int N,
+                             cudaStream_t stream) {
+  const int64_t k_tiles = (int64_t(K) + 31) / 32;
+  const dim3 grid(unsigned((int64_t(N) + 31) / 32), unsigned(k_tiles < 65535 ? k_tiles : 65535));
+  transpose_kernel<<<grid, dim3(32, 8), 0, stream>>>(B, ldb, Bt, ldbt, K, N);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tf32_kernel(const CUtensorMap& tmap_a, const CUtensorMap& tmap_bt, int M, int N,
+                               int K, float* C, int64_t ldc, int group_m, uint32_t* status,
+                               uint64_t limit, cudaStream_t stream) {
+  const int tiles_m = (M + kTfBM - 1) / kTfBM, tiles_n = (N + kTfBN - 1) / kTfBN;
+  tf32_kernel<<<tiles_m * tiles_n, kTfThreads, kTfSmem, stream>>>(
+      tmap_a, tmap_bt, M, N, K, C, ldc, tiles_m, tiles_n, group_m, status, limit);
+  return cudaGetLastError();
+}
+
+}  // namespace gb300

@@ -62,12 +62,15 @@ struct TileCfg {
   static constexpr int kProducers = 32 * kProducerWarps;
   static constexpr int NT = kConsumers + kProducers;
   static constexpr int kCtasPerSm = CTAS;
-  // Registers: the launch gives every thread R0; the producer warpgroup then
-  // hands registers to the consumer warpgroups (setmaxnreg), keeping the total.
+  // Registers: the launch gives every thread R0; when R0 is short of what a
+  // consumer needs, the producer warpgroup hands registers to the consumer
+  // warpgroups (setmaxnreg), keeping the block's total.
   static constexpr int kRegsLaunch = (65536 / (CTAS * NT)) / 8 * 8;
+  static constexpr bool kHandOver = kRegsLaunch < 232;
   static constexpr int kRegsProducer = PRODUCER_REGS;
   static constexpr int kRegsConsumer =
-      ((NT * kRegsLaunch - kProducers * kRegsProducer) / kConsumers) / 8 * 8;
+      kHandOver ? ((NT * kRegsLaunch - kProducers * kRegsProducer) / kConsumers) / 8 * 8
+                : kRegsLaunch;
   static constexpr int BM = WARPS_M * kWarpM;
   static constexpr int BN = WARPS_N * kWarpN;
   static constexpr int BK = 16;  // one 64-byte swizzle span of A per row
@@ -94,9 +97,11 @@ struct TileCfg {
   static_assert(BM <= 256 && BN <= 256, "TMA box dimensions are at most 256");
   static_assert(kBStageBytes % 1024 == 0 && kAStagingBytes % 512 == 0,
                 "stages keep the 64-byte swizzle period (512 bytes) aligned");
-  static_assert(kConsumers * kRegsConsumer + kProducers * kRegsProducer <= NT * kRegsLaunch,
+  static_assert(!kHandOver ||
+                    kConsumers * kRegsConsumer + kProducers * kRegsProducer <= NT * kRegsLaunch,
                 "register hand-over must stay within the launch allocation");
-  static_assert(kRegsConsumer <= 256 && kRegsConsumer >= kRegsLaunch, "consumer register budget");
+  static_assert(!kHandOver || (kRegsConsumer <= 256 && kRegsConsumer >= kRegsLaunch),
+                "consumer register budget");
 };
 
 // The compiled tile configurations (index = TileConfig id).
@@ -104,8 +109,8 @@ using Cfg0 = TileCfg<4, 2, 16, 4, 4, false, 1>;      // 128 x 256 tile, 8 + 4 wa
 using Cfg1 = TileCfg<4, 1, 16, 4, 4, false, 2, 40>;  // 128 x 128 tile, 4 + 4 warps, 2 CTAs / SM
 using Cfg2 = TileCfg<4, 2, 16, 4, 4, true, 1>;       // Cfg0 with fragment double buffering
 using Cfg3 = TileCfg<4, 2, 8, 4, 4, true, 1>;        // 128 x 128 tile, 8 + 4 warps, 8x8 patch
-using Cfg4 = TileCfg<4, 1, 16, 3, 3, false, 2, 40>;  // Cfg1 with a shallower ring
-using Cfg5 = TileCfg<4, 1, 16, 6, 2, false, 2, 40>;  // Cfg1 with a deeper B / A ring
+using Cfg4 = TileCfg<4, 1, 16, 4, 4, true, 1>;       // 128 x 128 tile, 4 + 4 warps, 8x16 patch
+using Cfg5 = TileCfg<4, 1, 16, 4, 4, false, 1>;      // Cfg4 without double buffering
 
 template <class F>
 auto with_cfg(int id, F&& f) {
@@ -243,7 +248,7 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
 
   if (warp >= T::kConsumerWarps) {
     // ================================================ producer warpgroup
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(T::kRegsProducer));
+    if constexpr (T::kHandOver) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(T::kRegsProducer));
     const int pw = warp - T::kConsumerWarps;  // this warp owns A rows [32 pw, 32 pw + 32)
     uint64_t* my_astage = astage + pw * T::S2;
     float* my_staging = sAst + pw * T::S2 * T::kAStagingFloats;
@@ -332,7 +337,7 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
   }
 
   // ======================================================= consumer warps
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(T::kRegsConsumer));
+  if constexpr (T::kHandOver) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(T::kRegsConsumer));
   const int tr = lane / T::kTC, tc = lane % T::kTC;
   const int wm = warp % T::kWarpsM, wn = warp / T::kWarpsM;
   const int a_frag = wm * T::kWarpM + 4 * tr;  // + 16 g + kAStride kk

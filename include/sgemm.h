@@ -98,6 +98,25 @@ int sgemm_select_variant(int64_t M, int64_t N, int64_t K, const float *A, int64_
 size_t sgemm_workspace_size(int variant, int64_t M, int64_t N, int64_t K);
 
 /*
+ * Opt-in TF32 tensor-core mode: C = A * B with the products formed from TF32
+ * inputs (FP32 exponent, 10 fraction bits) by tcgen05.mma and accumulated in
+ * FP32.  Not an FP32 result: its error is bounded by about 2^-10 of
+ * sum_k |A[m,k] B[k,n]| per element instead of K * 2^-24 of it; integer
+ * inputs below 2^11 in magnitude whose partial sums stay below 2^24 are still
+ * exact.  TF32 is the tensor-core precision the pages contrast with FP32
+ * ("Beyond Kernel 7", section "The operation: GEMM and the precision of the
+ * comparison"; "cuSgemm", Kernel 7).
+ *
+ * Same arguments and ownership as sgemm().  A and C must be 16-byte aligned
+ * with lda and ldc multiples of 4 (else SGEMM_ERR_INVALID_VALUE); B may have
+ * any stride.  B is first copied transposed into the per-(device, stream)
+ * workspace (N * round_up(K, 4) floats), which may grow with cudaMalloc as
+ * for sgemm().
+ */
+sgemm_status_t sgemm_tf32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                          const float *B, int64_t ldb, float *C, int64_t ldc, cudaStream_t stream);
+
+/*
  * Reads, then clears, the device status word of the current device after
  * synchronising `stream`: SGEMM_OK, or SGEMM_ERR_TIMEOUT if a kernel gave up
  * waiting since the last query.  *detail (may be NULL) receives a code that

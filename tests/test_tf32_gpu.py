@@ -1,0 +1,111 @@
+"""GPU parity of the opt-in TF32 tensor-core mode (``sgemm_tf32``) against the oracle.
+
+TF32 keeps FP32's exponent and 10 of its 23 fraction bits, so each input
+carries a relative error below 2^-10 (truncation; half that if rounded) and
+each product below 2^-9 + 2^-20.  With FP32 accumulation in any order the
+per-element error is then at most (2^-9 + 2^-20 + 2K 2^-24) sum_k |A B|; the
+test allows twice that.  Integers of magnitude <= 8 are exact in TF32, so
+integer inputs whose partial sums stay below 2^24 must match exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import dense_fp32_gemm_03_gb300 as sg
+from dense_fp32_gemm_03_gb300 import workloads
+
+from parity import check_exact
+
+pytestmark = pytest.mark.gpu
+
+
+def tf32_bound(K, E):
+    return (2.0 ** -8 + 4.0 * K * 2.0 ** -24) * E
+
+
+def check_tf32(C_gpu, C_ref, E, K, what):
+    C_gpu = np.asarray(C_gpu, dtype=np.float64)
+    assert np.all(np.isfinite(C_gpu)), f"{what}: non-finite output"
+    err = np.abs(C_gpu - C_ref)
+    lim = tf32_bound(K, E)
+    bad = err > lim
+    assert not np.any(bad), (f"{what}: {int(bad.sum())} elements outside the TF32 bound; "
+                             f"worst excess {(err - lim).max():.3e}")
+    return float((err / np.maximum(E, 1e-30)).max())
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    yield
+    assert sg.query_device_status() == (0, 0)
+
+
+def test_tf32_single_tile_integers_exact():
+    g = torch.Generator().manual_seed(3)
+    A = torch.randint(-8, 9, (128, 32), generator=g).float()
+    B = torch.randint(-8, 9, (32, 256), generator=g).float()
+    C = sg.sgemm_tf32(A.cuda(), B.cuda())
+    torch.cuda.synchronize()
+    ref, _ = oracle.sgemm_f64(A, B, with_abs=False)
+    check_exact(C.cpu().numpy(), ref, "tf32 one tile")
+
+
+def test_tf32_integer_workload_exact():
+    w = workloads.SMALL_256_INT
+    A, B = workloads.operands(w)
+    C = sg.sgemm_tf32(A.cuda(), B.cuda())
+    torch.cuda.synchronize()
+    ref, _ = oracle.sgemm_f64(A, B, with_abs=False)
+    check_exact(C.cpu().numpy(), ref, "tf32 int 256^3")
+
+
+@pytest.mark.parametrize("w", [workloads.SMALL_256, workloads.SQUARE_1024], ids=lambda w: w.name)
+def test_tf32_within_bound_full(w):
+    A, B = workloads.operands(w)
+    C = sg.sgemm_tf32(A.cuda(), B.cuda())
+    torch.cuda.synchronize()
+    ref, E = oracle.sgemm_f64(A, B)
+    worst = check_tf32(C.cpu().numpy(), ref, E, w.K, w.name)
+    assert worst > 0.0  # TF32 is not FP32: some rounding must show
+
+
+@pytest.mark.parametrize("w", [workloads.SQUARE_4096, workloads.LONG_K], ids=lambda w: w.name)
+def test_tf32_within_bound_sampled(w):
+    A, B = workloads.operands(w)
+    C = sg.sgemm_tf32(A.cuda(), B.cuda())
+    torch.cuda.synchronize()
+    r, c = workloads.sample_indices(w.M, w.N, 2048, w.seed)
+    ref, E = oracle.sgemm_entries_f64(A, B, r.numpy(), c.numpy())
+    check_tf32(C[r.cuda(), c.cuda()].cpu().numpy(), ref, E, w.K, w.name)
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1), (5, 7, 3), (127, 129, 65), (300, 520, 200),
+                                   (1000, 1000, 100), (130, 4, 1001), (257, 300, 33)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_tf32_ragged_shapes_and_k_tails(shape):
+    M, N, K = shape
+    lda = (K + 3) // 4 * 4                      # A's row stride must be a multiple of 4
+    A_big = workloads.matrix(M, lda, "normal", M + N, 0)
+    A = A_big[:, :K]
+    B = workloads.matrix(K, N, "normal", M + N, 1)   # B may have any stride
+    ldc = (N + 3) // 4 * 4
+    C_big = torch.full((M, ldc), float("nan"), device="cuda")
+    C = C_big[:, :N]
+    sg.sgemm_tf32(A.cuda() if A.is_contiguous() else A_big.cuda()[:, :K], B.cuda(), out=C)
+    torch.cuda.synchronize()
+    ref, E = oracle.sgemm_f64(np.ascontiguousarray(A.numpy()), B)
+    check_tf32(C.cpu().numpy(), ref, E, K, f"tf32 {shape}")
+    if ldc > N:
+        assert bool(torch.isnan(C_big[:, N:]).all()), "wrote past N"
+
+
+def test_tf32_rejects_misaligned_a():
+    A = torch.ones(64, 66, device="cuda")[:, 1:]     # 4-byte offset
+    B = torch.ones(65, 64, device="cuda")
+    with pytest.raises(sg.SgemmError):
+        sg.sgemm_tf32(A, B)
