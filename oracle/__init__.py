@@ -59,6 +59,9 @@ def _load():
             lib.ref_sgemm_f64.restype = ctypes.c_int
             lib.ref_sgemm_entries_f64.argtypes = [i64, i64, i64, fp, i64, fp, i64, i64, lp, lp, dp, dp]
             lib.ref_sgemm_entries_f64.restype = ctypes.c_int
+            lib.ref_sgemm_ex_f64.argtypes = [ctypes.c_int, i64, i64, i64, ctypes.c_double, fp, i64, fp,
+                                             i64, ctypes.c_double, fp, i64, dp, i64]
+            lib.ref_sgemm_ex_f64.restype = ctypes.c_int
             lib.ref_set_threads.argtypes = [ctypes.c_int]
             lib.ref_set_threads.restype = None
             lib.ref_max_threads.argtypes = []
@@ -132,6 +135,46 @@ def sgemm_entries_f64(A, B, rows, cols):
     if st != 0:
         raise ValueError(f"ref_sgemm_entries_f64 rejected its arguments (status {st})")
     return c, e
+
+
+def sgemm_ex_f64(A, B, alpha=1.0, beta=0.0, C0=None, col_major=False):
+    """alpha * (A . B) + beta * C0 in float64 (M x N, row-major result).
+
+    With ``col_major`` the float32 arrays are column-major: pass them as numpy
+    arrays in Fortran order (A: M x K, B: K x N, C0: M x N).  beta == 0 never
+    reads C0.
+    """
+    def prep(x, name):
+        if hasattr(x, "detach"):
+            x = x.detach().numpy()
+        x = np.asarray(x)
+        if x.dtype != np.float32 or x.ndim != 2:
+            raise ValueError(f"{name}: expected a 2-D float32 array")
+        if col_major:
+            x = np.asfortranarray(x)
+            return x, max(x.shape[0], 1)
+        x = np.ascontiguousarray(x)
+        return x, max(x.shape[1], 1)
+    A, lda = prep(A, "A")
+    B, ldb = prep(B, "B")
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: {A.shape} x {B.shape}")
+    if beta != 0.0:
+        C0, ldc = prep(C0, "C0")
+        if C0.shape != (M, N):
+            raise ValueError("C0 has the wrong shape")
+        c0p = _fptr(C0)
+    else:
+        ldc, c0p = max(M if col_major else N, 1), None
+    out = np.zeros((M, N), dtype=np.float64)
+    st = _load().ref_sgemm_ex_f64(int(bool(col_major)), M, N, K, float(alpha), _fptr(A), lda,
+                                  _fptr(B), ldb, float(beta), c0p, ldc,
+                                  out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), max(N, 1))
+    if st != 0:
+        raise ValueError(f"ref_sgemm_ex_f64 rejected its arguments (status {st})")
+    return out
 
 
 def set_threads(n: int) -> None:

@@ -105,6 +105,40 @@ int ref_sgemm_entries_f64(int64_t M, int64_t N, int64_t K, const float *A, int64
   return REF_OK;
 }
 
+/*
+ * The general form with scaling and either storage order.  The epilogue of
+ * "Vectorized Memory Access: Pushing CUDA SGEMM to 29 TFLOPS on H100", section
+ * 5, and "2D Block Tiling: Scaling Matrix Multiplication on NVIDIA H100",
+ * section 5, writes C[m, n] = alpha * (sum_k A[m, k] B[k, n]) + beta * C[m, n].
+ * Here C0 holds the old C (it may be NULL when beta == 0, which never reads
+ * it, so a NaN there does not propagate) and the result goes to Cout, all in
+ * double.  col_major != 0 means element (r, c) of a matrix with leading
+ * dimension ld sits at base[r + c * ld] instead of base[r * ld + c].
+ */
+int ref_sgemm_ex_f64(int col_major, int64_t M, int64_t N, int64_t K, double alpha,
+                     const float *A, int64_t lda, const float *B, int64_t ldb, double beta,
+                     const float *C0, int64_t ldc, double *Cout, int64_t ldo) {
+  if (M < 0 || N < 0 || K < 0) return REF_INVALID;
+  if (M == 0 || N == 0) return REF_OK;
+  if (Cout == NULL || ldo < N) return REF_INVALID;
+  if (beta != 0.0 && C0 == NULL) return REF_INVALID;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t m = 0; m < M; ++m) {
+    for (int64_t n = 0; n < N; ++n) {
+      double s = 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        const float a = col_major ? A[m + k * lda] : A[m * lda + k];
+        const float b = col_major ? B[k + n * ldb] : B[k * ldb + n];
+        s += (double)a * (double)b;
+      }
+      double r = alpha * s;
+      if (beta != 0.0) r += beta * (double)(col_major ? C0[m + n * ldc] : C0[m * ldc + n]);
+      Cout[m * ldo + n] = r;  /* the double result is always row-major */
+    }
+  }
+  return REF_OK;
+}
+
 /* Thread control for timing: 0 or less leaves the OpenMP default. */
 void ref_set_threads(int n) {
 #ifdef _OPENMP

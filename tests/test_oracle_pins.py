@@ -266,3 +266,39 @@ def test_integer_workload_partial_sums_stay_exact():
     assert w.K * 8 * 8 < 2 ** 24
     _, E = oracle.sgemm_f64(A, B)
     assert E.max() < 2 ** 24
+
+
+# ------------------------------------------------- the scaled, two-layout form
+def test_ex_reduces_to_the_plain_definition():
+    rng = _rng(11)
+    A = rng.standard_normal((9, 13)).astype(np.float32)
+    B = rng.standard_normal((13, 6)).astype(np.float32)
+    plain = oracle.sgemm_f64(A, B, with_abs=False)[0]
+    assert np.array_equal(oracle.sgemm_ex_f64(A, B), plain)
+    # A power-of-two alpha scales exactly.
+    assert np.array_equal(oracle.sgemm_ex_f64(A, B, alpha=-4.0), -4.0 * plain)
+
+
+def test_ex_beta_reads_c_and_beta_zero_ignores_it():
+    rng = _rng(12)
+    A = rng.integers(-8, 9, size=(7, 5)).astype(np.float32)
+    B = rng.integers(-8, 9, size=(5, 4)).astype(np.float32)
+    C0 = rng.integers(-8, 9, size=(7, 4)).astype(np.float32)
+    expect = 3.0 * (A.astype(np.int64) @ B.astype(np.int64)) - 2.0 * C0
+    assert np.array_equal(oracle.sgemm_ex_f64(A, B, alpha=3.0, beta=-2.0, C0=C0), expect)
+    nan_c = np.full((7, 4), np.nan, dtype=np.float32)
+    assert np.array_equal(oracle.sgemm_ex_f64(A, B, alpha=1.0, beta=0.0, C0=nan_c),
+                          (A.astype(np.int64) @ B.astype(np.int64)).astype(np.float64))
+    # alpha = 0 leaves beta * C0 (A and B only multiply a zero).
+    assert np.array_equal(oracle.sgemm_ex_f64(A, B, alpha=0.0, beta=0.5, C0=C0), 0.5 * C0)
+
+
+def test_ex_column_major_is_the_same_product():
+    rng = _rng(13)
+    A = rng.standard_normal((6, 11)).astype(np.float32)
+    B = rng.standard_normal((11, 8)).astype(np.float32)
+    C0 = rng.standard_normal((6, 8)).astype(np.float32)
+    row = oracle.sgemm_ex_f64(A, B, alpha=0.5, beta=2.0, C0=C0)
+    col = oracle.sgemm_ex_f64(np.asfortranarray(A), np.asfortranarray(B), alpha=0.5, beta=2.0,
+                              C0=np.asfortranarray(C0), col_major=True)
+    assert np.array_equal(row, col)
