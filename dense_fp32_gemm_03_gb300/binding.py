@@ -23,7 +23,7 @@ VARIANTS = {"guarded": GUARDED, "tiled": TILED, "streamk": STREAMK,
 EXPORTS = ("sgemm", "sgemm_variant", "sgemm_select_variant", "sgemm_workspace_size",
            "sgemm_query_device_status", "sgemm_release_workspaces", "sgemm_status_string",
            "sgemm_variant_name", "sgemm_debug_expire_wait", "sgemm_streamk_static",
-           "sgemm_tf32")
+           "sgemm_tf32", "sgemm_ex")
 
 
 class SgemmError(RuntimeError):
@@ -77,6 +77,9 @@ def load(path: str | None = None):
         lib.sgemm_streamk_static.restype = st
         lib.sgemm_tf32.argtypes = gemm_args
         lib.sgemm_tf32.restype = st
+        f32 = ctypes.c_float
+        lib.sgemm_ex.argtypes = [ctypes.c_int, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
+        lib.sgemm_ex.restype = st
         _lib = lib
         return lib
 
@@ -144,6 +147,40 @@ def sgemm(A, B, out=None, variant: int = AUTO, stream=None):
     if st != OK:
         raise SgemmError(st, "sgemm")
     return out
+
+
+ROW_MAJOR, COL_MAJOR = 0, 1
+
+
+def sgemm_ex(A, B, C, alpha=1.0, beta=0.0, layout=ROW_MAJOR, stream=None):
+    """C = alpha * A @ B + beta * C in place, for 2-D float32 CUDA tensors.
+
+    ``layout`` ROW_MAJOR: tensors with unit column stride; COL_MAJOR: tensors
+    with unit row stride (e.g. ``x.t().contiguous().t()``), as BLAS expects.
+    """
+    import torch
+
+    def ld(t, name):
+        if t.device.type != "cuda" or t.dtype != torch.float32 or t.dim() != 2:
+            raise ValueError(f"{name} must be a 2-D float32 CUDA tensor")
+        if layout == ROW_MAJOR:
+            if t.shape[1] > 1 and t.stride(1) != 1:
+                raise ValueError(f"{name} must have unit column stride")
+            return max(t.stride(0), t.shape[1], 1)
+        if t.shape[0] > 1 and t.stride(0) != 1:
+            raise ValueError(f"{name} must have unit row stride")
+        return max(t.stride(1), t.shape[0], 1)
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2 or tuple(C.shape) != (M, N):
+        raise ValueError(f"shapes do not match: {tuple(A.shape)} @ {tuple(B.shape)} -> {tuple(C.shape)}")
+    with torch.cuda.device(A.device):
+        st = load().sgemm_ex(int(layout), M, N, K, float(alpha), A.data_ptr(), ld(A, "A"),
+                             B.data_ptr(), ld(B, "B"), float(beta), C.data_ptr(), ld(C, "C"),
+                             _stream_handle(A.device, stream))
+    if st != OK:
+        raise SgemmError(st, "sgemm_ex")
+    return C
 
 
 def sgemm_tf32(A, B, out=None, stream=None):

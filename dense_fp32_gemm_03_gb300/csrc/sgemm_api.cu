@@ -301,8 +301,10 @@ sgemm_status_t get_workspace(int dev, cudaStream_t stream, const Plan& p, void**
   return get_workspace_bytes(dev, stream, p.workspace_bytes(), out);
 }
 
-sgemm_status_t run(int variant, int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
-                   const float* B, int64_t ldb, float* C, int64_t ldc, cudaStream_t stream) {
+sgemm_status_t run(int variant, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                   int64_t lda, const float* B, int64_t ldb, float beta, float* C, int64_t ldc,
+                   cudaStream_t stream) {
+  const bool scaled = !(alpha == 1.0f && beta == 0.0f);
   sgemm_status_t st = validate(M, N, K, A, lda, B, ldb, C, ldc);
   if (st != SGEMM_OK) return st;
   if (variant < SGEMM_VARIANT_AUTO || variant >= SGEMM_VARIANT_COUNT) return SGEMM_ERR_INVALID_VALUE;
@@ -311,12 +313,15 @@ sgemm_status_t run(int variant, int64_t M, int64_t N, int64_t K, const float* A,
   st = device_state(&ds, &dev);
   if (st != SGEMM_OK) return st;
   if (M == 0 || N == 0) return SGEMM_OK;
-  if (K == 0) {
-    return gb300::launch_zero_fill(M, N, C, ldc, stream) == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+  if (K == 0 || alpha == 0.0f) {  // the product term vanishes: C = beta * C
+    const cudaError_t e = scaled ? gb300::launch_scale(M, N, C, ldc, beta, stream)
+                                 : gb300::launch_zero_fill(M, N, C, ldc, stream);
+    return e == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
   }
   if (variant == SGEMM_VARIANT_AUTO) variant = select_variant(M, N, K, A, lda, B, ldb, C, ldc, *ds);
   if (variant == SGEMM_VARIANT_GUARDED) {
-    return gb300::launch_guarded_kernel(M, N, K, A, lda, B, ldb, C, ldc, stream) == cudaSuccess
+    return gb300::launch_guarded_kernel(M, N, K, A, lda, B, ldb, C, ldc, scaled ? 1 : 0, alpha,
+                                        beta, stream) == cudaSuccess
                ? SGEMM_OK
                : SGEMM_ERR_LAUNCH;
   }
@@ -363,6 +368,9 @@ sgemm_status_t run(int variant, int64_t M, int64_t N, int64_t K, const float* A,
   args.partials = ws ? reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes) : nullptr;
   args.status = ds->status;
   args.wait_limit_ns = kDefaultWaitLimitNs;
+  args.scaled = scaled ? 1 : 0;
+  args.alpha = alpha;
+  args.beta = beta;
   return gb300::launch_tile_kernel(p.cfg, tmap_a, tmap_b, args, p.sc, p.grid, stream) == cudaSuccess
              ? SGEMM_OK
              : SGEMM_ERR_LAUNCH;
@@ -374,13 +382,24 @@ extern "C" {
 
 sgemm_status_t sgemm(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
                      int64_t ldb, float* C, int64_t ldc, cudaStream_t stream) {
-  return run(SGEMM_VARIANT_AUTO, M, N, K, A, lda, B, ldb, C, ldc, stream);
+  return run(SGEMM_VARIANT_AUTO, M, N, K, 1.0f, A, lda, B, ldb, 0.0f, C, ldc, stream);
+}
+
+sgemm_status_t sgemm_ex(int layout, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                        int64_t lda, const float* B, int64_t ldb, float beta, float* C, int64_t ldc,
+                        cudaStream_t stream) {
+  if (layout == SGEMM_ROW_MAJOR)
+    return run(SGEMM_VARIANT_AUTO, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+  if (layout != SGEMM_COL_MAJOR) return SGEMM_ERR_INVALID_VALUE;
+  // Column-major C = A B is row-major C^T = B^T A^T over the same memory: the
+  // column-major B (K x N, ld ldb) read row-major is B^T (N x K), and so on.
+  return run(SGEMM_VARIANT_AUTO, N, M, K, alpha, B, ldb, A, lda, beta, C, ldc, stream);
 }
 
 sgemm_status_t sgemm_variant(int variant, int64_t M, int64_t N, int64_t K, const float* A,
                              int64_t lda, const float* B, int64_t ldb, float* C, int64_t ldc,
                              cudaStream_t stream) {
-  return run(variant, M, N, K, A, lda, B, ldb, C, ldc, stream);
+  return run(variant, M, N, K, 1.0f, A, lda, B, ldb, 0.0f, C, ldc, stream);
 }
 
 int sgemm_select_variant(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,

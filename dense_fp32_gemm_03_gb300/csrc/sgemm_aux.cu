@@ -21,7 +21,7 @@ constexpr int kGBM = 64, kGBN = 64, kGBK = 16, kGThreads = 256;
 __global__ void __launch_bounds__(kGThreads)
     guarded_kernel(int64_t M, int64_t N, int64_t K, const float* __restrict__ A, int64_t lda,
                    const float* __restrict__ B, int64_t ldb, float* __restrict__ C, int64_t ldc,
-                   int64_t tiles_n) {
+                   int64_t tiles_n, int scaled, float alpha, float beta) {
   __shared__ float As[kGBK][kGBM];
   __shared__ float Bs[kGBK][kGBN];
   const int64_t tile = blockIdx.x;
@@ -65,7 +65,12 @@ __global__ void __launch_bounds__(kGThreads)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int64_t gn = n0 + tx + 16 * j;
-      if (gn < N) C[gm * ldc + gn] = acc[i][j];
+      if (gn >= N) continue;
+      float* p = C + gm * ldc + gn;
+      if (!scaled)
+        *p = acc[i][j];
+      else
+        *p = beta != 0.f ? fmaf(beta, *p, alpha * acc[i][j]) : alpha * acc[i][j];
     }
   }
 }
@@ -75,6 +80,16 @@ __global__ void zero_fill_kernel(int64_t M, int64_t N, float* __restrict__ C, in
   for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
        i += int64_t(gridDim.x) * blockDim.x) {
     C[(i / N) * ldc + (i % N)] = 0.f;
+  }
+}
+
+// C = beta * C: the product term vanishes (K == 0 or alpha == 0).
+__global__ void scale_kernel(int64_t M, int64_t N, float* __restrict__ C, int64_t ldc, float beta) {
+  const int64_t total = M * N;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    float* p = C + (i / N) * ldc + (i % N);
+    *p = beta != 0.f ? beta * *p : 0.f;
   }
 }
 
@@ -96,13 +111,13 @@ __global__ void expire_probe_kernel(uint32_t* status, uint64_t limit_ns) {
 }  // namespace
 
 cudaError_t launch_guarded_kernel(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
-                                  const float* B, int64_t ldb, float* C, int64_t ldc,
-                                  cudaStream_t stream) {
+                                  const float* B, int64_t ldb, float* C, int64_t ldc, int scaled,
+                                  float alpha, float beta, cudaStream_t stream) {
   const int64_t tiles_m = (M + kGBM - 1) / kGBM, tiles_n = (N + kGBN - 1) / kGBN;
   const int64_t tiles = tiles_m * tiles_n;
   if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
   guarded_kernel<<<unsigned(tiles), kGThreads, 0, stream>>>(M, N, K, A, lda, B, ldb, C, ldc,
-                                                            tiles_n);
+                                                            tiles_n, scaled, alpha, beta);
   return cudaGetLastError();
 }
 
@@ -111,6 +126,15 @@ cudaError_t launch_zero_fill(int64_t M, int64_t N, float* C, int64_t ldc, cudaSt
   int64_t blocks = (total + 255) / 256;
   if (blocks > 65536) blocks = 65536;
   zero_fill_kernel<<<unsigned(blocks), 256, 0, stream>>>(M, N, C, ldc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale(int64_t M, int64_t N, float* C, int64_t ldc, float beta,
+                         cudaStream_t stream) {
+  const int64_t total = M * N;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 65536) blocks = 65536;
+  scale_kernel<<<unsigned(blocks), 256, 0, stream>>>(M, N, C, ldc, beta);
   return cudaGetLastError();
 }
 

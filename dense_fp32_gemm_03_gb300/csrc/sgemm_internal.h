@@ -47,6 +47,10 @@ struct GemmArgs {
   int32_t* counters;    // one arrival counter per split tile, zero on entry, zero on exit
   uint32_t* status;     // device status word: [0] = sgemm_status_t, [1] = WaitSite
   uint64_t wait_limit_ns;
+  // Epilogue C = alpha * acc + beta * C when `scaled` (beta == 0 never reads C);
+  // C = acc otherwise.
+  int32_t scaled;
+  float alpha, beta;
 };
 
 // Tile configurations of the pipelined kernel (compiled instances, by id).
@@ -89,10 +93,13 @@ cudaError_t launch_tf32_kernel(const CUtensorMap& tmap_a, const CUtensorMap& tma
                                uint64_t limit, cudaStream_t stream);
 
 cudaError_t launch_guarded_kernel(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
-                                  const float* B, int64_t ldb, float* C, int64_t ldc,
-                                  cudaStream_t stream);
+                                  const float* B, int64_t ldb, float* C, int64_t ldc, int scaled,
+                                  float alpha, float beta, cudaStream_t stream);
 
 cudaError_t launch_zero_fill(int64_t M, int64_t N, float* C, int64_t ldc, cudaStream_t stream);
+
+// C = beta * C (beta == 0: C = 0 without reading it).
+cudaError_t launch_scale(int64_t M, int64_t N, float* C, int64_t ldc, float beta, cudaStream_t stream);
 
 cudaError_t launch_expire_probe(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
 

@@ -429,10 +429,31 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
       const int r = j / Q, h = j % Q;
       return make_float4(acc[r][2 * h].x, acc[r][2 * h].y, acc[r][2 * h + 1].x, acc[r][2 * h + 1].y);
     };
+    // alpha / beta epilogue: C = alpha * v + beta * C; beta == 0 never reads C.
+    auto finish = [&](float4 v, const float* p, int ncols) {
+      float4 r = make_float4(args.alpha * v.x, args.alpha * v.y, args.alpha * v.z, args.alpha * v.w);
+      if (args.beta != 0.f) {
+        float4 c;
+        if (ncols >= 4) {
+          c = *reinterpret_cast<const float4*>(p);
+        } else {
+          c.x = ncols > 0 ? p[0] : 0.f;
+          c.y = ncols > 1 ? p[1] : 0.f;
+          c.z = ncols > 2 ? p[2] : 0.f;
+          c.w = 0.f;
+        }
+        r.x = fmaf(args.beta, c.x, r.x);
+        r.y = fmaf(args.beta, c.y, r.y);
+        r.z = fmaf(args.beta, c.z, r.z);
+        r.w = fmaf(args.beta, c.w, r.w);
+      }
+      return r;
+    };
     auto store_c = [&](int j, float4 v) {
       const int row = out_row(j / Q), col = out_col(j % Q);
       if (row >= M) return;
       float* p = args.C + int64_t(row) * args.ldc + col;
+      if (args.scaled) v = finish(v, p, N - col);
       if (col + 4 <= N) {
         *reinterpret_cast<float4*>(p) = v;
       } else {
@@ -444,7 +465,7 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
     };
 
     if (u.t_sk < 0 || (u.kb == 0 && u.ke == sc.iters_per_tile)) {
-      if (m0 + T::BM <= M && n0 + T::BN <= N) {
+      if (m0 + T::BM <= M && n0 + T::BN <= N && !args.scaled) {
 #pragma unroll
         for (int j = 0; j < T::kOutVec; ++j) {
           float* p = args.C + int64_t(out_row(j / Q)) * args.ldc + out_col(j % Q);

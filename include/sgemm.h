@@ -73,6 +73,28 @@ typedef enum {
 sgemm_status_t sgemm(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
                      const float *B, int64_t ldb, float *C, int64_t ldc, cudaStream_t stream);
 
+/* Storage order of the operands of sgemm_ex(). */
+typedef enum {
+  SGEMM_ROW_MAJOR = 0, /* element (r, c) at base[r * ld + c] */
+  SGEMM_COL_MAJOR = 1  /* element (r, c) at base[r + c * ld] */
+} sgemm_layout_t;
+
+/*
+ * C = alpha * A * B + beta * C, the general form whose epilogue the pages
+ * print ("Vectorized Memory Access ...", section 5: alpha * acc + beta * C;
+ * "2D Block Tiling ...", section 5).  `layout` (an sgemm_layout_t) applies to
+ * A, B and C alike; leading dimensions are row strides for SGEMM_ROW_MAJOR
+ * (lda >= K, ldb >= N, ldc >= N) and column strides for SGEMM_COL_MAJOR
+ * (lda >= M, ldb >= K, ldc >= M).  beta == 0 never reads C (NaN there does
+ * not propagate); alpha == 0 or K == 0 gives C = beta * C without reading A
+ * or B.  Column-major problems run as the row-major C^T = B^T A^T over the
+ * same memory.  Otherwise as sgemm(): same kernels, selector, workspace and
+ * error behaviour; sgemm(...) is sgemm_ex(SGEMM_ROW_MAJOR, ..., 1, ..., 0, ...).
+ */
+sgemm_status_t sgemm_ex(int layout, int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                        int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                        int64_t ldc, cudaStream_t stream);
+
 /*
  * As sgemm() but forces `variant` (an sgemm_variant_t).  A fast variant given
  * operands it cannot take (misaligned pointer or stride) returns
