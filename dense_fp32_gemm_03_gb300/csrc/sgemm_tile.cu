@@ -49,7 +49,7 @@ namespace {
 constexpr uint32_t kStatusTimeout = 3;  // SGEMM_ERR_TIMEOUT
 
 template <int WARPS_M, int WARPS_N, int TN, int STAGES, int ASTAGES, bool DB, int CTAS,
-          int PRODUCER_REGS = 56>
+          int PRODUCER_REGS = 56, bool PAIRED_COLS = false>
 struct TileCfg {
   static constexpr int kTR = 4, kTC = 8;    // lane grid of a consumer warp: rows x columns
   static constexpr int kTM = 8, kTN = TN;   // outputs per thread
@@ -68,6 +68,11 @@ struct TileCfg {
   static constexpr int kRegsLaunch = (65536 / (CTAS * NT)) / 8 * 8;
   static constexpr bool kHandOver = kRegsLaunch < 232;
   static constexpr int kRegsProducer = PRODUCER_REGS;
+  // Lane layout.  false: a quarter-warp is one lane row (one A address, eight
+  // B addresses).  true: a quarter-warp is four lane rows x two lane columns,
+  // each column's four lanes adjacent (four A addresses, two B addresses),
+  // which costs fewer shared-memory wavefronts per k step.
+  static constexpr bool kPairedCols = PAIRED_COLS;
   static constexpr int kRegsConsumer =
       kHandOver ? ((NT * kRegsLaunch - kProducers * kRegsProducer) / kConsumers) / 8 * 8
                 : kRegsLaunch;
@@ -105,12 +110,12 @@ struct TileCfg {
 };
 
 // The compiled tile configurations (index = TileConfig id).
-using Cfg0 = TileCfg<4, 2, 16, 4, 4, false, 1>;      // 128 x 256 tile, 8 + 4 warps, 8x16 patch
-using Cfg1 = TileCfg<4, 1, 16, 4, 4, false, 2, 40>;  // 128 x 128 tile, 4 + 4 warps, 2 CTAs / SM
-using Cfg2 = TileCfg<4, 2, 16, 4, 4, true, 1>;       // Cfg0 with fragment double buffering
-using Cfg3 = TileCfg<4, 2, 8, 4, 4, true, 1>;        // 128 x 128 tile, 8 + 4 warps, 8x8 patch
-using Cfg4 = TileCfg<4, 1, 16, 4, 4, true, 1>;       // 128 x 128 tile, 4 + 4 warps, 8x16 patch
-using Cfg5 = TileCfg<4, 1, 16, 4, 4, false, 1>;      // Cfg4 without double buffering
+using Cfg0 = TileCfg<4, 2, 16, 4, 4, false, 1, 56, true>;   // 128 x 256 tile, 8 + 4 warps, 8x16 patch
+using Cfg1 = TileCfg<4, 2, 16, 4, 4, false, 1>;             // Cfg0, one-row quarter-warps
+using Cfg2 = TileCfg<4, 2, 16, 4, 4, true, 1, 56, true>;    // Cfg1 with fragment double buffering
+using Cfg3 = TileCfg<4, 2, 8, 4, 4, true, 1>;               // 128 x 128 tile, 8 + 4 warps, 8x8 patch
+using Cfg4 = TileCfg<4, 2, 8, 4, 4, true, 1, 56, true>;     // Cfg3, paired-column lane layout
+using Cfg5 = TileCfg<4, 2, 8, 4, 4, false, 1, 56, true>;    // Cfg4 without double buffering
 
 template <class F>
 auto with_cfg(int id, F&& f) {
@@ -207,7 +212,9 @@ __device__ __forceinline__ int sk_owner(const Sched& sc, int64_t i) {
   return sc.sk_extra + int((i - big) / sc.sk_base);
 }
 
-template <class T>
+// SCALED: the epilogue applies alpha / beta (a separate instance, so that the
+// plain C = A * B kernel carries no scaling code).
+template <class T, bool SCALED>
 __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
     tile_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                 const GemmArgs args, const Sched sc) {
@@ -338,7 +345,8 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
 
   // ======================================================= consumer warps
   if constexpr (T::kHandOver) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(T::kRegsConsumer));
-  const int tr = lane / T::kTC, tc = lane % T::kTC;
+  const int tr = T::kPairedCols ? (lane & 3) : lane / T::kTC;
+  const int tc = T::kPairedCols ? (((lane >> 3) << 1) | ((lane >> 2) & 1)) : lane % T::kTC;
   const int wm = warp % T::kWarpsM, wn = warp / T::kWarpsM;
   const int a_frag = wm * T::kWarpM + 4 * tr;  // + 16 g + kAStride kk
   const int b_frag = wn * T::kWarpN + 4 * tc;      // + 32 h + BN kk
@@ -453,7 +461,7 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
       const int row = out_row(j / Q), col = out_col(j % Q);
       if (row >= M) return;
       float* p = args.C + int64_t(row) * args.ldc + col;
-      if (args.scaled) v = finish(v, p, N - col);
+      if constexpr (SCALED) v = finish(v, p, N - col);
       if (col + 4 <= N) {
         *reinterpret_cast<float4*>(p) = v;
       } else {
@@ -465,7 +473,7 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
     };
 
     if (u.t_sk < 0 || (u.kb == 0 && u.ke == sc.iters_per_tile)) {
-      if (m0 + T::BM <= M && n0 + T::BN <= N && !args.scaled) {
+      if (m0 + T::BM <= M && n0 + T::BN <= N && !SCALED) {
 #pragma unroll
         for (int j = 0; j < T::kOutVec; ++j) {
           float* p = args.C + int64_t(out_row(j / Q)) * args.ldc + out_col(j % Q);
@@ -533,12 +541,14 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
 
 template <class T>
 int prepare() {
-  if (cudaFuncSetAttribute(tile_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(tile_kernel<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(T::kSmem)) != cudaSuccess ||
+      cudaFuncSetAttribute(tile_kernel<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(T::kSmem)) != cudaSuccess)
     return -1;
   int blocks = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, tile_kernel<T>, T::NT, T::kSmem) !=
-      cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, tile_kernel<T, false>, T::NT,
+                                                    T::kSmem) != cudaSuccess)
     return -1;
   return blocks;
 }
@@ -564,7 +574,10 @@ cudaError_t launch_tile_kernel(TileConfig cfg, const CUtensorMap& tmap_a, const 
                                cudaStream_t stream) {
   return with_cfg(cfg, [&](auto c) {
     using T = decltype(c);
-    tile_kernel<T><<<grid, T::NT, T::kSmem, stream>>>(tmap_a, tmap_b, args, sched);
+    if (args.scaled)
+      tile_kernel<T, true><<<grid, T::NT, T::kSmem, stream>>>(tmap_a, tmap_b, args, sched);
+    else
+      tile_kernel<T, false><<<grid, T::NT, T::kSmem, stream>>>(tmap_a, tmap_b, args, sched);
     return cudaGetLastError();
   });
 }
