@@ -233,6 +233,54 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Vectorized variant for 16-byte-aligned B with ldb % 4 == 0 (and Bt likewise):
+// 64 x 64 tiles moved as 128-bit loads and stores.
+__global__ void __launch_bounds__(256)
+    transpose_vec_kernel(const float* __restrict__ B, int64_t ldb, float* __restrict__ Bt,
+                         int64_t ldbt, int K, int N) {
+  __shared__ float tile[64][65];
+  const int64_t n0 = int64_t(blockIdx.x) * 64;
+  const int64_t k_tiles = (int64_t(K) + 63) / 64;
+  for (int64_t ky = blockIdx.y; ky < k_tiles; ky += gridDim.y) {
+    const int64_t k0 = ky * 64;
+    for (int i = threadIdx.x; i < 64 * 16; i += 256) {
+      const int r = i / 16, c = 4 * (i % 16);
+      const int64_t k = k0 + r, n = n0 + c;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (k < K) {
+        const float* p = B + k * ldb + n;
+        if (n + 3 < N) {
+          v = *reinterpret_cast<const float4*>(p);
+        } else {
+          if (n + 0 < N) v.x = p[0];
+          if (n + 1 < N) v.y = p[1];
+          if (n + 2 < N) v.z = p[2];
+        }
+      }
+      tile[r][c] = v.x;
+      tile[r][c + 1] = v.y;
+      tile[r][c + 2] = v.z;
+      tile[r][c + 3] = v.w;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 64 * 16; i += 256) {
+      const int r = i / 16, c = 4 * (i % 16);
+      const int64_t n = n0 + r, k = k0 + c;
+      if (n >= N) continue;
+      const float4 v = make_float4(tile[c][r], tile[c + 1][r], tile[c + 2][r], tile[c + 3][r]);
+      float* p = Bt + n * ldbt + k;
+      if (k + 3 < K) {
+        *reinterpret_cast<float4*>(p) = v;
+      } else {
+        if (k + 0 < K) p[0] = v.x;
+        if (k + 1 < K) p[1] = v.y;
+        if (k + 2 < K) p[2] = v.z;
+      }
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace
 
 size_t tf32_smem_bytes() { return kTfSmem; }
@@ -253,9 +301,17 @@ int tf32_prepare() {
 
 cudaError_t launch_transpose(const float* B, int64_t ldb, float* Bt, int64_t ldbt, int K, int N,
                              cudaStream_t stream) {
-  const int64_t k_tiles = (int64_t(K) + 31) / 32;
-  const dim3 grid(unsigned((int64_t(N) + 31) / 32), unsigned(k_tiles < 65535 ? k_tiles : 65535));
-  transpose_kernel<<<grid, dim3(32, 8), 0, stream>>>(B, ldb, Bt, ldbt, K, N);
+  const bool vec = (reinterpret_cast<uintptr_t>(B) & 15u) == 0 && ldb % 4 == 0 &&
+                   (reinterpret_cast<uintptr_t>(Bt) & 15u) == 0 && ldbt % 4 == 0;
+  if (vec) {
+    const int64_t k_tiles = (int64_t(K) + 63) / 64;
+    const dim3 grid(unsigned((int64_t(N) + 63) / 64), unsigned(k_tiles < 65535 ? k_tiles : 65535));
+    transpose_vec_kernel<<<grid, 256, 0, stream>>>(B, ldb, Bt, ldbt, K, N);
+  } else {
+    const int64_t k_tiles = (int64_t(K) + 31) / 32;
+    const dim3 grid(unsigned((int64_t(N) + 31) / 32), unsigned(k_tiles < 65535 ? k_tiles : 65535));
+    transpose_kernel<<<grid, dim3(32, 8), 0, stream>>>(B, ldb, Bt, ldbt, K, N);
+  }
   return cudaGetLastError();
 }
 
