@@ -293,3 +293,45 @@ def test_workspace_reuse_across_split_layouts():
             torch.cuda.synchronize()
             assert bool(torch.isfinite(out).all()), f"{(M, N, K)} variant {v}: tiles not written"
             check_within_bound(out[r.cuda(), c.cuda()].cpu().numpy(), ref, E, K, f"{(M, N, K)} v{v}")
+
+
+def test_concurrent_streams_use_separate_workspaces():
+    """Two Stream-K calls in flight at once on two streams: each keeps its own workspace."""
+    shapes = [(1536, 1536, 1536, 81), (1024, 1024, 2048, 82)]
+    ops, outs, streams = [], [], [torch.cuda.Stream(), torch.cuda.Stream()]
+    for M, N, K, seed in shapes:
+        ops.append((workloads.matrix(M, K, "normal", seed, 0), workloads.matrix(K, N, "normal", seed, 1)))
+    dev = [(A.cuda(), B.cuda()) for A, B in ops]
+    torch.cuda.synchronize()
+    for rep in range(3):
+        for (A, B), s in zip(dev, streams):
+            with torch.cuda.stream(s):
+                outs.append(sg.sgemm(A, B, variant=sg.STREAMK))
+    torch.cuda.synchronize()
+    for idx, ((A, B), (M, N, K, seed)) in enumerate(zip(ops, shapes)):
+        r, c = workloads.sample_indices(M, N, 1024, seed)
+        ref, E = oracle.sgemm_entries_f64(A, B, r.numpy(), c.numpy())
+        for rep in range(3):
+            got = outs[2 * rep + idx][r.cuda(), c.cuda()].cpu().numpy()
+            check_within_bound(got, ref, E, K, f"stream {idx} rep {rep}")
+
+
+def test_graph_capture_and_replay():
+    """After one call has sized the stream's workspace, sgemm() captures into a CUDA graph."""
+    w = workloads.SQUARE_1024
+    A_h, B_h = workloads.operands(w)
+    A, B = A_h.cuda(), B_h.cuda()
+    C = torch.empty(w.M, w.N, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        sg.sgemm(A, B, out=C)          # warm-up: workspace for this stream exists now
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        sg.sgemm(A, B, out=C)
+    C.fill_(float("nan"))
+    A.copy_(workloads.matrix(w.M, w.K, w.dist, 4242, 0))   # new inputs, same buffers
+    graph.replay()
+    torch.cuda.synchronize()
+    ref, E = oracle.sgemm_f64(A.cpu(), B_h)
+    check_within_bound(C.cpu().numpy(), ref, E, w.K, "graph replay")
