@@ -34,6 +34,12 @@ constexpr int kMinSkIters = 4;  // Stream-K shares shorter than this many k-tile
 // counters are: counters are zero at allocation and every call leaves them zero.
 constexpr size_t kCounterBytes = 16384;
 constexpr int64_t kMaxSplitTiles = kCounterBytes / 4;
+// Cost-model constants of the guarded kernel and of the operand copies
+// (measured on GB300).
+constexpr double kGuardedTflops = 23.0;     // large products
+constexpr double kGuardedStepUs = 1.6;      // one 16-deep step of a CTA (a global-load round trip)
+constexpr double kGuardedCtasPerSm = 4.0;   // 256 threads x 64 registers
+constexpr double kCopyBytesPerUs = 4.5e6;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -153,6 +159,10 @@ bool fast_path_ok(const float* A, int64_t lda, const float* B, int64_t ldb, cons
          ldc % 4 == 0;
 }
 
+bool operand_ok(const void* p, int64_t ld) { return aligned16(p) && ld % 4 == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
 struct Plan {
   int variant = -1;
   TileConfig cfg = 0;
@@ -161,6 +171,39 @@ struct Plan {
   size_t partial_bytes = 0;
   size_t workspace_bytes() const { return partial_bytes ? kCounterBytes + partial_bytes : 0; }
 };
+
+// The staged variant: an operand the TMA-fed kernels cannot read in place (a
+// base address that is not 16-byte aligned, or a row stride that is not a
+// multiple of 4 floats) is first copied into the workspace with row stride
+// round_up(cols, 4); a C of that kind is written with 4-byte stores.  The
+// copies sit after the counter region and the partial tiles.
+struct Staging {
+  bool a = false, b = false;
+  int64_t lda = 0, ldb = 0;     // row strides of the copies
+  size_t a_off = 0, b_off = 0;  // byte offsets of the copies in the workspace
+  size_t bytes = 0;             // workspace bytes, copies included
+};
+
+Staging make_staging(const Plan& p, int64_t M, int64_t N, int64_t K, bool stage_a, bool stage_b) {
+  Staging sg;
+  sg.bytes = p.workspace_bytes();
+  if (!stage_a && !stage_b) return sg;
+  size_t off = kCounterBytes + round_up(p.partial_bytes, 256);
+  if (stage_a) {
+    sg.a = true;
+    sg.lda = (K + 3) / 4 * 4;
+    sg.a_off = off;
+    off += round_up(size_t(M) * size_t(sg.lda) * 4, 256);
+  }
+  if (stage_b) {
+    sg.b = true;
+    sg.ldb = (N + 3) / 4 * 4;
+    sg.b_off = off;
+    off += round_up(size_t(K) * size_t(sg.ldb) * 4, 256);
+  }
+  sg.bytes = off;
+  return sg;
+}
 
 bool is_fast(int v) {
   return v == SGEMM_VARIANT_TILED || v == SGEMM_VARIANT_STREAMK ||
@@ -248,11 +291,30 @@ double plan_cost_us(const Plan& p, const DeviceState& ds) {
   return 10.0 + iters * ktile_us + fixup;
 }
 
-// The selector: aligned operands take the pipelined variant with the lowest
-// estimated time; the rest take the guarded kernel.
-int select_variant(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
-                   int64_t ldb, const float* C, int64_t ldc, const DeviceState& ds) {
-  if (!fast_path_ok(A, lda, B, ldb, C, ldc)) return SGEMM_VARIANT_GUARDED;
+// Estimated duration (microseconds) of the bounds-checked kernel, fitted to
+// measured GB300 timings: small products are bound by the latency of its
+// unpipelined 16-deep steps (one global round trip each, per wave of 64 x 64
+// tiles), large ones by its arithmetic rate.
+double guarded_cost_us(int64_t M, int64_t N, int64_t K, const DeviceState& ds) {
+  const double tiles = double((M + 63) / 64) * double((N + 63) / 64);
+  const double waves = std::ceil(tiles / (double(ds.sms) * kGuardedCtasPerSm));
+  const double latency = kGuardedStepUs * double((K + 15) / 16) * waves;
+  const double arithmetic = 2.0 * double(M) * double(N) * double(K) / (kGuardedTflops * 1e6);
+  return 5.0 + (latency > arithmetic ? latency : arithmetic);
+}
+
+// Estimated cost (microseconds) of copying the operands that need it: one
+// launch, then 8 bytes of traffic per element.
+double staging_cost_us(int64_t M, int64_t N, int64_t K, bool stage_a, bool stage_b) {
+  if (!stage_a && !stage_b) return 0.0;
+  double elems = 0.0;
+  if (stage_a) elems += double(M) * double(K);
+  if (stage_b) elems += double(K) * double(N);
+  return 4.0 + 8.0 * elems / kCopyBytesPerUs;
+}
+
+// The pipelined variant with the lowest estimated time for this shape.
+int select_fast(int64_t M, int64_t N, int64_t K, const DeviceState& ds, double* cost_out) {
   int best = SGEMM_VARIANT_STREAMK;
   double best_cost = 1e300;
   const int candidates[4] = {SGEMM_VARIANT_STREAMK, SGEMM_VARIANT_STREAMK_SMALL,
@@ -266,7 +328,21 @@ int select_variant(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
       best = v;
     }
   }
+  if (cost_out) *cost_out = best_cost;
   return best;
+}
+
+// The selector: aligned operands take the pipelined variant with the lowest
+// estimated time; the rest take the staged variant or the bounds-checked
+// kernel, whichever is estimated faster.
+int select_variant(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
+                   int64_t ldb, const float* C, int64_t ldc, const DeviceState& ds) {
+  double cost = 0.0;
+  const int fast = select_fast(M, N, K, ds, &cost);
+  if (fast_path_ok(A, lda, B, ldb, C, ldc)) return fast;
+  const double staged =
+      cost + staging_cost_us(M, N, K, !operand_ok(A, lda), !operand_ok(B, ldb));
+  return staged < guarded_cost_us(M, N, K, ds) ? SGEMM_VARIANT_STAGED : SGEMM_VARIANT_GUARDED;
 }
 
 sgemm_status_t get_workspace_bytes(int dev, cudaStream_t stream, size_t need, void** out) {
@@ -301,6 +377,35 @@ sgemm_status_t get_workspace(int dev, cudaStream_t stream, const Plan& p, void**
   return get_workspace_bytes(dev, stream, p.workspace_bytes(), out);
 }
 
+// Tensor maps of the pipelined kernel: A (K fastest) in boxes of 16 x
+// a_box_rows with the 64-byte swizzle, B (N fastest) in boxes of BN x 16.
+sgemm_status_t encode_operands(const TileShape& ts, int64_t M, int64_t N, int64_t K, const float* A,
+                               int64_t lda, const float* B, int64_t ldb, CUtensorMap* tmap_a,
+                               CUtensorMap* tmap_b) {
+  std::memset(tmap_a, 0, sizeof(*tmap_a));
+  std::memset(tmap_b, 0, sizeof(*tmap_b));
+  const cuuint32_t estr[2] = {1, 1};
+  {
+    const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(M)};
+    const cuuint64_t strides[1] = {cuuint64_t(lda) * 4};
+    const cuuint32_t box[2] = {cuuint32_t(ts.bk), cuuint32_t(ts.a_box_rows)};
+    if (g_encode(tmap_a, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(A), dims, strides,
+                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return SGEMM_ERR_LAUNCH;
+  }
+  {
+    const cuuint64_t dims[2] = {cuuint64_t(N), cuuint64_t(K)};
+    const cuuint64_t strides[1] = {cuuint64_t(ldb) * 4};
+    const cuuint32_t box[2] = {cuuint32_t(ts.bn), cuuint32_t(ts.bk)};
+    if (g_encode(tmap_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(B), dims, strides,
+                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return SGEMM_ERR_LAUNCH;
+  }
+  return SGEMM_OK;
+}
+
 sgemm_status_t run(int variant, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
                    int64_t lda, const float* B, int64_t ldb, float beta, float* C, int64_t ldc,
                    cudaStream_t stream) {
@@ -325,43 +430,48 @@ sgemm_status_t run(int variant, int64_t M, int64_t N, int64_t K, float alpha, co
                ? SGEMM_OK
                : SGEMM_ERR_LAUNCH;
   }
-  if (!fast_path_ok(A, lda, B, ldb, C, ldc)) return SGEMM_ERR_INVALID_VALUE;
+  const bool staged = variant == SGEMM_VARIANT_STAGED;
+  if (staged)
+    variant = select_fast(M, N, K, *ds, nullptr);
+  else if (!fast_path_ok(A, lda, B, ldb, C, ldc))
+    return SGEMM_ERR_INVALID_VALUE;
   Plan p;
   if (!make_plan(variant, M, N, K, *ds, &p)) return SGEMM_ERR_UNSUPPORTED;
   const TileShape ts = gb300::tile_shape(p.cfg);
-
-  CUtensorMap tmap_a, tmap_b;
-  std::memset(&tmap_a, 0, sizeof(tmap_a));
-  std::memset(&tmap_b, 0, sizeof(tmap_b));
-  const cuuint32_t estr[2] = {1, 1};
-  {
-    const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(M)};
-    const cuuint64_t strides[1] = {cuuint64_t(lda) * 4};
-    const cuuint32_t box[2] = {cuuint32_t(ts.bk), cuuint32_t(ts.a_box_rows)};
-    if (g_encode(&tmap_a, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(A), dims, strides,
-                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return SGEMM_ERR_LAUNCH;
-  }
-  {
-    const cuuint64_t dims[2] = {cuuint64_t(N), cuuint64_t(K)};
-    const cuuint64_t strides[1] = {cuuint64_t(ldb) * 4};
-    const cuuint32_t box[2] = {cuuint32_t(ts.bn), cuuint32_t(ts.bk)};
-    if (g_encode(&tmap_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(B), dims, strides,
-                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return SGEMM_ERR_LAUNCH;
-  }
+  const Staging sg =
+      make_staging(p, M, N, K, staged && !operand_ok(A, lda), staged && !operand_ok(B, ldb));
 
   void* ws = nullptr;
-  st = get_workspace(dev, stream, p, &ws);
+  st = get_workspace_bytes(dev, stream, sg.bytes, &ws);
   if (st != SGEMM_OK) return st;
+  const float* a_in = A;
+  const float* b_in = B;
+  int64_t lda_in = lda, ldb_in = ldb;
+  gb300::PackCopy copy_a{}, copy_b{};
+  if (sg.a) {
+    float* a_copy = reinterpret_cast<float*>(static_cast<char*>(ws) + sg.a_off);
+    copy_a = gb300::PackCopy{A, a_copy, M, K, lda, sg.lda};
+    a_in = a_copy;
+    lda_in = sg.lda;
+  }
+  if (sg.b) {
+    float* b_copy = reinterpret_cast<float*>(static_cast<char*>(ws) + sg.b_off);
+    copy_b = gb300::PackCopy{B, b_copy, K, N, ldb, sg.ldb};
+    b_in = b_copy;
+    ldb_in = sg.ldb;
+  }
+  if ((sg.a || sg.b) && gb300::launch_pack(copy_a, copy_b, stream) != cudaSuccess)
+    return SGEMM_ERR_LAUNCH;
+  CUtensorMap tmap_a, tmap_b;
+  st = encode_operands(ts, M, N, K, a_in, lda_in, b_in, ldb_in, &tmap_a, &tmap_b);
+  if (st != SGEMM_OK) return st;
+
   gb300::GemmArgs args{};
   args.M = int(M);
   args.N = int(N);
   args.K = int(K);
-  args.A = A;
-  args.lda = lda;
+  args.A = a_in;
+  args.lda = lda_in;
   args.C = C;
   args.ldc = ldc;
   args.counters = static_cast<int32_t*>(ws);
@@ -371,6 +481,7 @@ sgemm_status_t run(int variant, int64_t M, int64_t N, int64_t K, float alpha, co
   args.scaled = scaled ? 1 : 0;
   args.alpha = alpha;
   args.beta = beta;
+  args.c_scalar = operand_ok(C, ldc) ? 0 : 1;
   return gb300::launch_tile_kernel(p.cfg, tmap_a, tmap_b, args, p.sc, p.grid, stream) == cudaSuccess
              ? SGEMM_OK
              : SGEMM_ERR_LAUNCH;
@@ -419,9 +530,12 @@ size_t sgemm_workspace_size(int variant, int64_t M, int64_t N, int64_t K) {
     const float* p = reinterpret_cast<const float*>(uintptr_t(256));
     variant = select_variant(M, N, K, p, (K + 3) / 4 * 4, p, (N + 3) / 4 * 4, p, (N + 3) / 4 * 4, *ds);
   }
+  const bool staged = variant == SGEMM_VARIANT_STAGED;
+  if (staged) variant = select_fast(M, N, K, *ds, nullptr);
   Plan p;
   if (!make_plan(variant, M, N, K, *ds, &p)) return 0;
-  return p.workspace_bytes();
+  // The staged variant is sized for copies of both A and B.
+  return make_staging(p, M, N, K, staged, staged).bytes;
 }
 
 sgemm_status_t sgemm_tf32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
@@ -535,6 +649,7 @@ const char* sgemm_variant_name(int v) {
     case SGEMM_VARIANT_STREAMK: return "streamk";
     case SGEMM_VARIANT_TILED_SMALL: return "tiled_small";
     case SGEMM_VARIANT_STREAMK_SMALL: return "streamk_small";
+    case SGEMM_VARIANT_STAGED: return "staged";
   }
   return "unknown";
 }
@@ -611,27 +726,8 @@ extern "C" sgemm_status_t sgemm_streamk_static(int64_t M, int64_t N, int64_t K, 
   const TileShape ts = gb300::tile_shape(p.cfg);
 
   CUtensorMap tmap_a, tmap_b;
-  std::memset(&tmap_a, 0, sizeof(tmap_a));
-  std::memset(&tmap_b, 0, sizeof(tmap_b));
-  const cuuint32_t estr[2] = {1, 1};
-  {
-    const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(M)};
-    const cuuint64_t strides[1] = {cuuint64_t(lda) * 4};
-    const cuuint32_t box[2] = {cuuint32_t(ts.bk), cuuint32_t(ts.a_box_rows)};
-    if (g_encode(&tmap_a, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(A), dims, strides,
-                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return SGEMM_ERR_LAUNCH;
-  }
-  {
-    const cuuint64_t dims[2] = {cuuint64_t(N), cuuint64_t(K)};
-    const cuuint64_t strides[1] = {cuuint64_t(ldb) * 4};
-    const cuuint32_t box[2] = {cuuint32_t(ts.bn), cuuint32_t(ts.bk)};
-    if (g_encode(&tmap_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(B), dims, strides,
-                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return SGEMM_ERR_LAUNCH;
-  }
+  st = encode_operands(ts, M, N, K, A, lda, B, ldb, &tmap_a, &tmap_b);
+  if (st != SGEMM_OK) return st;
 
   // The array keeps whatever the previous call left: the arrival counters of
   // this call's split tiles must start at zero.

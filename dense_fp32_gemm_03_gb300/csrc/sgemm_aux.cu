@@ -1,6 +1,8 @@
 // sgemm_aux.cu -- the small kernels around the pipelined one:
 //  * the bounds-checked GEMM for operands the fast kernels cannot take
 //    (misaligned pointers, strides that are not multiples of 4);
+//  * the copy of an operand the TMA-fed kernels cannot read in place into an
+//    aligned buffer;
 //  * the zero fill of C for K == 0 (the empty sum);
 //  * the wait-expiry probe behind sgemm_debug_expire_wait().
 #include <cuda_runtime.h>
@@ -75,6 +77,44 @@ __global__ void __launch_bounds__(kGThreads)
   }
 }
 
+// One warp copies one 128-column segment of one row: 4-byte loads and stores
+// that are consecutive across the warp, so any source alignment and stride
+// coalesce.  The source is read once, hence the streaming loads.  One launch
+// serves up to two matrices (A and B): warps [0, jobs[0].rows * segs) copy
+// the first, the rest the second.
+constexpr int kPackSeg = 128;
+
+struct PackJob {
+  const float* src;
+  float* dst;
+  int64_t rows, cols, ld_src, ld_dst, segs;
+};
+
+__device__ __forceinline__ void pack_segment(const PackJob& j, int64_t w, int lane) {
+  const int64_t r = w / j.segs, c0 = (w % j.segs) * kPackSeg + lane;
+  const float* s = j.src + r * j.ld_src;
+  float* d = j.dst + r * j.ld_dst;
+  float v[kPackSeg / 32];
+#pragma unroll
+  for (int i = 0; i < kPackSeg / 32; ++i) v[i] = c0 + 32 * i < j.cols ? __ldcs(s + c0 + 32 * i) : 0.f;
+#pragma unroll
+  for (int i = 0; i < kPackSeg / 32; ++i)
+    if (c0 + 32 * i < j.cols) d[c0 + 32 * i] = v[i];
+}
+
+__global__ void pack_kernel(PackJob j0, PackJob j1) {
+  const int lane = threadIdx.x & 31;
+  const int64_t n0 = j0.rows * j0.segs, total = n0 + j1.rows * j1.segs;
+  const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t w = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); w < total;
+       w += warps) {
+    if (w < n0)
+      pack_segment(j0, w, lane);
+    else
+      pack_segment(j1, w - n0, lane);
+  }
+}
+
 __global__ void zero_fill_kernel(int64_t M, int64_t N, float* __restrict__ C, int64_t ldc) {
   const int64_t total = M * N;
   for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
@@ -118,6 +158,22 @@ cudaError_t launch_guarded_kernel(int64_t M, int64_t N, int64_t K, const float* 
   if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
   guarded_kernel<<<unsigned(tiles), kGThreads, 0, stream>>>(M, N, K, A, lda, B, ldb, C, ldc,
                                                             tiles_n, scaled, alpha, beta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack(const PackCopy& first, const PackCopy& second, cudaStream_t stream) {
+  auto job = [](const PackCopy& c) {
+    PackJob j{c.src, c.dst, c.rows, c.cols, c.ld_src, c.ld_dst, 0};
+    if (c.rows > 0 && c.cols > 0) j.segs = (c.cols + kPackSeg - 1) / kPackSeg;
+    else j.rows = 0;
+    return j;
+  };
+  const PackJob j0 = job(first), j1 = job(second);
+  const int64_t warps = j0.rows * j0.segs + j1.rows * j1.segs;
+  if (warps == 0) return cudaSuccess;
+  int64_t blocks = (warps + 7) / 8;  // 8 warps per block
+  if (blocks > 65536) blocks = 65536;
+  pack_kernel<<<unsigned(blocks), 256, 0, stream>>>(j0, j1);
   return cudaGetLastError();
 }
 

@@ -51,6 +51,9 @@ struct GemmArgs {
   // C = acc otherwise.
   int32_t scaled;
   float alpha, beta;
+  // Nonzero when C is not 16-byte aligned or ldc is not a multiple of 4: every
+  // access to C is then a 4-byte one.
+  int32_t c_scalar;
 };
 
 // Tile configurations of the pipelined kernel (compiled instances, by id).
@@ -95,6 +98,17 @@ cudaError_t launch_tf32_kernel(const CUtensorMap& tmap_a, const CUtensorMap& tma
 cudaError_t launch_guarded_kernel(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
                                   const float* B, int64_t ldb, float* C, int64_t ldc, int scaled,
                                   float alpha, float beta, cudaStream_t stream);
+
+// dst (rows x cols, row stride ld_dst, 16-byte aligned, ld_dst a multiple of
+// 4) = src (any row stride and alignment).  Columns cols..ld_dst-1 of dst are
+// left as they are.  rows == 0 or cols == 0: nothing to copy.
+struct PackCopy {
+  const float* src;
+  float* dst;
+  int64_t rows, cols, ld_src, ld_dst;
+};
+// Both copies in one launch.
+cudaError_t launch_pack(const PackCopy& first, const PackCopy& second, cudaStream_t stream);
 
 cudaError_t launch_zero_fill(int64_t M, int64_t N, float* C, int64_t ldc, cudaStream_t stream);
 

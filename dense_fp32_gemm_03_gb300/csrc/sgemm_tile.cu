@@ -437,18 +437,20 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
       const int r = j / Q, h = j % Q;
       return make_float4(acc[r][2 * h].x, acc[r][2 * h].y, acc[r][2 * h + 1].x, acc[r][2 * h + 1].y);
     };
+    // A C that is not 16-byte aligned row by row is read and written 4 bytes at a time.
+    const bool c_vec = args.c_scalar == 0;
     // alpha / beta epilogue: C = alpha * v + beta * C; beta == 0 never reads C.
     auto finish = [&](float4 v, const float* p, int ncols) {
       float4 r = make_float4(args.alpha * v.x, args.alpha * v.y, args.alpha * v.z, args.alpha * v.w);
       if (args.beta != 0.f) {
         float4 c;
-        if (ncols >= 4) {
+        if (ncols >= 4 && c_vec) {
           c = *reinterpret_cast<const float4*>(p);
         } else {
           c.x = ncols > 0 ? p[0] : 0.f;
           c.y = ncols > 1 ? p[1] : 0.f;
           c.z = ncols > 2 ? p[2] : 0.f;
-          c.w = 0.f;
+          c.w = ncols > 3 ? p[3] : 0.f;
         }
         r.x = fmaf(args.beta, c.x, r.x);
         r.y = fmaf(args.beta, c.y, r.y);
@@ -462,7 +464,7 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
       if (row >= M) return;
       float* p = args.C + int64_t(row) * args.ldc + col;
       if constexpr (SCALED) v = finish(v, p, N - col);
-      if (col + 4 <= N) {
+      if (col + 4 <= N && c_vec) {
         *reinterpret_cast<float4*>(p) = v;
       } else {
         if (col + 0 < N) p[0] = v.x;
@@ -473,7 +475,7 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
     };
 
     if (u.t_sk < 0 || (u.kb == 0 && u.ke == sc.iters_per_tile)) {
-      if (m0 + T::BM <= M && n0 + T::BN <= N && !SCALED) {
+      if (m0 + T::BM <= M && n0 + T::BN <= N && !SCALED && c_vec) {
 #pragma unroll
         for (int j = 0; j < T::kOutVec; ++j) {
           float* p = args.C + int64_t(out_row(j / Q)) * args.ldc + out_col(j % Q);

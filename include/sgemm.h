@@ -60,15 +60,21 @@ typedef enum {
   SGEMM_VARIANT_STREAMK = 2,   /* persistent CTAs: whole tiles in full waves, the rest split over K */
   SGEMM_VARIANT_TILED_SMALL = 3,   /* pipelined 128x128 tiles, one output tile per CTA */
   SGEMM_VARIANT_STREAMK_SMALL = 4, /* Stream-K schedule over 128x128 tiles */
-  SGEMM_VARIANT_COUNT = 5
+  SGEMM_VARIANT_STAGED = 5,    /* any stride and alignment: unaligned A, B copied aligned first */
+  SGEMM_VARIANT_COUNT = 6
 } sgemm_variant_t;
 
 /*
  * C = A * B.  M, N, K >= 0; lda >= K, ldb >= N, ldc >= N (elements).
  * M == 0 or N == 0: nothing to do, SGEMM_OK.  K == 0: C is filled with zeros
- * (the empty sum).  Any stride and alignment is accepted; the fast kernels
- * need 16-byte-aligned A, B, C and lda, ldb, ldc multiples of 4, and other
- * inputs take the bounds-checked kernel.
+ * (the empty sum).  Any stride and alignment is accepted.  The pipelined
+ * kernels read A and B by TMA, which needs 16-byte-aligned base addresses and
+ * row strides that are multiples of 4 floats.  An operand without that
+ * property (for instance a contiguous matrix with an odd number of columns)
+ * is either first copied into an aligned buffer in the workspace (the staged
+ * variant; a C without it is then written with 4-byte stores) or the whole
+ * product runs in the bounds-checked kernel, whichever the selector
+ * estimates to be faster: the staged variant for all but small products.
  */
 sgemm_status_t sgemm(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
                      const float *B, int64_t ldb, float *C, int64_t ldc, cudaStream_t stream);
@@ -96,9 +102,13 @@ sgemm_status_t sgemm_ex(int layout, int64_t M, int64_t N, int64_t K, float alpha
                         int64_t ldc, cudaStream_t stream);
 
 /*
- * As sgemm() but forces `variant` (an sgemm_variant_t).  A fast variant given
- * operands it cannot take (misaligned pointer or stride) returns
- * SGEMM_ERR_INVALID_VALUE without launching.
+ * As sgemm() but forces `variant` (an sgemm_variant_t).  The four pipelined
+ * variants (TILED, STREAMK, TILED_SMALL, STREAMK_SMALL) given operands they
+ * cannot take (a base address that is not 16-byte aligned or a row stride
+ * that is not a multiple of 4) return SGEMM_ERR_INVALID_VALUE without
+ * launching.  GUARDED and STAGED take any operands; STAGED copies only the
+ * operands that need it, into the per-(device, stream) workspace, and then
+ * runs the pipelined schedule the selector picks for the shape.
  */
 sgemm_status_t sgemm_variant(int variant, int64_t M, int64_t N, int64_t K, const float *A,
                              int64_t lda, const float *B, int64_t ldb, float *C, int64_t ldc,
@@ -114,8 +124,10 @@ int sgemm_select_variant(int64_t M, int64_t N, int64_t K, const float *A, int64_
 
 /*
  * Bytes of workspace the given variant (or the selected one, for
- * SGEMM_VARIANT_AUTO) needs for this shape on the current device; 0 when it
- * needs none.  Returns 0 for invalid arguments too.
+ * SGEMM_VARIANT_AUTO, assuming aligned operands) needs for this shape on the
+ * current device; 0 when it needs none.  For SGEMM_VARIANT_STAGED the figure
+ * includes copies of both A and B, the most that variant can need.  Returns 0
+ * for invalid arguments too.
  */
 size_t sgemm_workspace_size(int variant, int64_t M, int64_t N, int64_t K);
 

@@ -19,7 +19,7 @@ from parity import check_exact, check_within_bound
 pytestmark = pytest.mark.gpu
 
 FAST = [sg.TILED, sg.STREAMK, sg.TILED_SMALL, sg.STREAMK_SMALL]
-ALL_VARIANTS = [sg.GUARDED, *FAST]
+ALL_VARIANTS = [sg.GUARDED, *FAST, sg.STAGED]
 SENTINEL = float.fromhex("0x1.dead00p+100")
 
 
@@ -151,12 +151,12 @@ def test_row_strides_and_views():
         check_within_bound(C.cpu().numpy(), ref, E, 200, f"views variant {v}")
 
 
-def test_misaligned_pointer_takes_guarded_path():
+def test_misaligned_pointer_avoids_the_fast_variants():
     buf_a = workloads.matrix(1, 64 * 64 + 1, "uniform", 4, 0).cuda()
     A = buf_a[0, 1:].view(64, 64)  # 4-byte offset: not 16-byte aligned
     B = workloads.matrix(64, 64, "uniform", 4, 1).cuda()
     C = torch.empty(64, 64, device="cuda")
-    assert sg.select_variant(A, B, C) == sg.GUARDED
+    assert sg.select_variant(A, B, C) in (sg.GUARDED, sg.STAGED)
     with pytest.raises(sg.SgemmError):
         sg.sgemm(A, B, out=C, variant=sg.TILED)
     sg.sgemm(A, B, out=C)
