@@ -109,6 +109,14 @@ __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
 }
 
 // Records the first error of a launch in the device status word.
+// Load with acquire semantics at GPU scope: writes another CTA released
+// before storing this value are visible after it.
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void record_status(uint32_t* status, uint32_t code, uint32_t site) {
   if (atomicCAS(status, 0u, code) == 0u) status[1] = site;
 }

@@ -52,7 +52,8 @@ struct GemmArgs {
   int32_t scaled;
   float alpha, beta;
   // Nonzero when C is not 16-byte aligned or ldc is not a multiple of 4: every
-  // access to C is then a 4-byte one.
+  // access to C is then a 4-byte one (in the general epilogue, which also
+  // applies alpha and beta: alpha = 1, beta = 0 leave acc unchanged).
   int32_t c_scalar;
 };
 

@@ -98,6 +98,7 @@ struct TileCfg {
   static constexpr size_t kFlagOff = kBarOff + size_t(2 * S + kProducerWarps * S2) * 8;
   static constexpr size_t kSmem = kFlagOff + 16;
   static_assert(TN == 8 || TN == 16, "patch width");
+  static_assert(ASTAGES <= STAGES, "the prologue's B tiles must fit the empty ring");
   static_assert(kRowsPerProducer == 32, "each producer lane owns one row of the A tile");
   static_assert(BM <= 256 && BN <= 256, "TMA box dimensions are at most 256");
   static_assert(kBStageBytes % 1024 == 0 && kAStagingBytes % 512 == 0,
@@ -212,8 +213,10 @@ __device__ __forceinline__ int sk_owner(const Sched& sc, int64_t i) {
   return sc.sk_extra + int((i - big) / sc.sk_base);
 }
 
-// SCALED: the epilogue applies alpha / beta (a separate instance, so that the
-// plain C = A * B kernel carries no scaling code).
+// SCALED: the general epilogue, C = alpha * acc + beta * C with C read and
+// written 4 bytes at a time when it is not 16-byte aligned row by row (a
+// separate instance, so that the plain C = A * B kernel with aligned C
+// carries neither).
 template <class T, bool SCALED>
 __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
     tile_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
@@ -280,25 +283,35 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
                        (issue.u.kb + issue.j) * T::BK, m0 + pw * T::kRowsPerProducer,
                        &my_astage[slot]);
     };
-    // Prologue: this warp's first S2 A slices into its staging ring.
+    // The B tile of k-tile `c.j` of unit `c.u` into ring stage s.
+    auto issue_b = [&](const KCursor& c, uint32_t s) {
+      int m0, n0;
+      tile_mn(c.u, m0, n0);
+      dev::mbar_expect_tx(&full[s], T::kBStageBytes);
+      dev::tma_load_2d(sB + s * T::kBStageFloats, &tmap_b, n0, (c.u.kb + c.j) * T::BK, &full[s]);
+    };
+    // Prologue: this warp's first S2 A slices into its staging ring and, from
+    // warp 0, the B tiles of the same k-tiles (their ring stages start empty),
+    // each right behind its A slice so that the first stage fills as early
+    // as the copies allow.
     uint32_t issued = 0;
     for (int s = 0; s < T::S2 && issue.valid; ++s) {
-      if (lane == 0) issue_a(s);
+      if (lane == 0) {
+        issue_a(s);
+        if (pw == 0) issue_b(issue, s);
+      }
       ++issued;
       issue.advance(sc, ctas);
     }
+    const uint32_t b_issued = issued;
     uint32_t i = 0;
     for (; proc.valid; ++i) {
       const uint32_t s = i % T::S, n = i / T::S;
       const uint32_t s2 = i % T::S2, n2 = i / T::S2;
-      if (n > 0 && !dev::mbar_wait_abortable(&empty[s], (n - 1) & 1u, limit, s_abort))
-        fail(kWaitTileStage);
-      if (pw == 0 && lane == 0 && !*s_abort) {
-        int m0, n0;
-        tile_mn(proc.u, m0, n0);
-        dev::mbar_expect_tx(&full[s], T::kBStageBytes);
-        dev::tma_load_2d(sB + s * T::kBStageFloats, &tmap_b, n0, (proc.u.kb + proc.j) * T::BK,
-                         &full[s]);
+      if (i >= b_issued) {
+        if (n > 0 && !dev::mbar_wait_abortable(&empty[s], (n - 1) & 1u, limit, s_abort))
+          fail(kWaitTileStage);
+        if (pw == 0 && lane == 0 && !*s_abort) issue_b(proc, s);
       }
       if (!dev::mbar_wait_abortable(&my_astage[s2], n2 & 1u, limit, s_abort)) fail(kWaitTileStage);
       // Transpose this warp's 32 rows: staging [r][k] (64-byte swizzled rows:
@@ -437,8 +450,9 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
       const int r = j / Q, h = j % Q;
       return make_float4(acc[r][2 * h].x, acc[r][2 * h].y, acc[r][2 * h + 1].x, acc[r][2 * h + 1].y);
     };
-    // A C that is not 16-byte aligned row by row is read and written 4 bytes at a time.
-    const bool c_vec = args.c_scalar == 0;
+    // A C that is not 16-byte aligned row by row is read and written 4 bytes
+    // at a time; only the general (SCALED) instance carries that code.
+    const bool c_vec = SCALED ? args.c_scalar == 0 : true;
     // alpha / beta epilogue: C = alpha * v + beta * C; beta == 0 never reads C.
     auto finish = [&](float4 v, const float* p, int ncols) {
       float4 r = make_float4(args.alpha * v.x, args.alpha * v.y, args.alpha * v.z, args.alpha * v.w);
@@ -488,54 +502,89 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
       continue;
     }
 
-    // Split tile: publish this CTA's partial sums; the last CTA to arrive
-    // adds all partials in CTA order (deterministic) and writes C.
+    // Split tile: the CTAs that share it publish their partial sums and the
+    // last to arrive adds all partials in CTA order (deterministic) and
+    // writes C.  The CTA that owns the tile's first k-tiles keeps its partial
+    // in registers: if it finds every other sharer already arrived it is the
+    // last and publishes nothing; if it turns out last after publishing, it
+    // still adds from its registers.  Either way the sum is the same
+    // sequence of additions, so the result does not depend on who is last.
     const int64_t t_first_iter = int64_t(u.t_sk) * sc.iters_per_tile;
     const int c_first = sk_owner(sc, t_first_iter);
     const int c_last = sk_owner(sc, t_first_iter + sc.iters_per_tile - 1);
+    const int others = c_last - c_first;
     const int64_t tile_floats = int64_t(T::BM) * T::BN;
-    {
+    const bool own_first = cta == c_first;
+    bool last = false;
+    if (own_first) {
+      if (tid == 0) *s_last = dev::ld_acquire_gpu(args.counters + u.t_sk) == others ? 1 : 0;
+      dev::named_barrier(1, T::kConsumers);
+      last = *s_last != 0;
+      dev::named_barrier(1, T::kConsumers);  // s_last is rewritten below
+    }
+    if (!last) {
       float4* mine = reinterpret_cast<float4*>(args.partials + (u.t_sk + cta) * tile_floats);
 #pragma unroll
       for (int j = 0; j < T::kOutVec; ++j) __stcg(mine + j * T::kConsumers + tid, value(j));
+      __threadfence();
+      dev::named_barrier(1, T::kConsumers);
+      if (tid == 0) {
+        const int arrived = atomicAdd(args.counters + u.t_sk, 1);
+        *s_last = (arrived == others) ? 1 : 0;
+      }
+      dev::named_barrier(1, T::kConsumers);
+      last = *s_last != 0;
+      dev::named_barrier(1, T::kConsumers);  // s_last may be rewritten by the next split tile
     }
-    __threadfence();
-    dev::named_barrier(1, T::kConsumers);
-    if (tid == 0) {
-      const int arrived = atomicAdd(args.counters + u.t_sk, 1);
-      *s_last = (arrived == c_last - c_first) ? 1 : 0;
-    }
-    dev::named_barrier(1, T::kConsumers);
-    const bool last = *s_last != 0;
-    dev::named_barrier(1, T::kConsumers);  // s_last may be rewritten by the next split tile
     if (last) {
-      // Every partial, this CTA's included, is in the workspace: sum them in
-      // CTA order with all of a slot's loads in flight at once.
+      // Every other partial is in the workspace.
       __threadfence();
       const float4* base = reinterpret_cast<const float4*>(args.partials) + tid;
       const int64_t slot_vec = tile_floats / 4;
-      float4 sum[T::kOutVec];
-      {
-        const float4* src = base + (u.t_sk + c_first) * slot_vec;
-#pragma unroll
-        for (int j = 0; j < T::kOutVec; ++j) sum[j] = __ldcg(src + j * T::kConsumers);
-      }
+      if (own_first) {
+        // acc += partial, CTA after CTA, with a slot's loads in flight at once.
 #pragma unroll 1
-      for (int cc = c_first + 1; cc <= c_last; ++cc) {
-        const float4* src = base + (u.t_sk + cc) * slot_vec;
-        float4 v[T::kOutVec];
+        for (int cc = c_first + 1; cc <= c_last; ++cc) {
+          const float4* src = base + (u.t_sk + cc) * slot_vec;
+          float4 v[T::kOutVec];
 #pragma unroll
-        for (int j = 0; j < T::kOutVec; ++j) v[j] = __ldcg(src + j * T::kConsumers);
+          for (int j = 0; j < T::kOutVec; ++j) v[j] = __ldcg(src + j * T::kConsumers);
 #pragma unroll
-        for (int j = 0; j < T::kOutVec; ++j) {
-          sum[j].x += v[j].x;
-          sum[j].y += v[j].y;
-          sum[j].z += v[j].z;
-          sum[j].w += v[j].w;
+          for (int j = 0; j < T::kOutVec; ++j) {
+            const int r = j / Q, h = j % Q;
+            acc[r][2 * h].x += v[j].x;
+            acc[r][2 * h].y += v[j].y;
+            acc[r][2 * h + 1].x += v[j].z;
+            acc[r][2 * h + 1].y += v[j].w;
+          }
         }
-      }
 #pragma unroll
-      for (int j = 0; j < T::kOutVec; ++j) store_c(j, sum[j]);
+        for (int j = 0; j < T::kOutVec; ++j) store_c(j, value(j));
+      } else {
+        // Sum every partial, this CTA's included, in CTA order.
+        float4 sum[T::kOutVec];
+        {
+          const float4* src = base + (u.t_sk + c_first) * slot_vec;
+#pragma unroll
+          for (int j = 0; j < T::kOutVec; ++j) sum[j] = __ldcg(src + j * T::kConsumers);
+        }
+#pragma unroll 1
+        for (int cc = c_first + 1; cc <= c_last; ++cc) {
+          const float4* src = base + (u.t_sk + cc) * slot_vec;
+          float4 v[T::kOutVec];
+#pragma unroll
+          for (int j = 0; j < T::kOutVec; ++j) v[j] = __ldcg(src + j * T::kConsumers);
+#pragma unroll
+          for (int j = 0; j < T::kOutVec; ++j) {
+            sum[j].x += v[j].x;
+            sum[j].y += v[j].y;
+            sum[j].z += v[j].z;
+            sum[j].w += v[j].w;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < T::kOutVec; ++j) store_c(j, sum[j]);
+      }
       if (tid == 0) args.counters[u.t_sk] = 0;
     }
   }
@@ -576,7 +625,7 @@ cudaError_t launch_tile_kernel(TileConfig cfg, const CUtensorMap& tmap_a, const 
                                cudaStream_t stream) {
   return with_cfg(cfg, [&](auto c) {
     using T = decltype(c);
-    if (args.scaled)
+    if (args.scaled || args.c_scalar)
       tile_kernel<T, true><<<grid, T::NT, T::kSmem, stream>>>(tmap_a, tmap_b, args, sched);
     else
       tile_kernel<T, false><<<grid, T::NT, T::kSmem, stream>>>(tmap_a, tmap_b, args, sched);
