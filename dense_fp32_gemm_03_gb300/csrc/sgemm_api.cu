@@ -27,8 +27,7 @@ __device__ uint32_t g_status_word[2];
 
 constexpr int64_t kInt32Max = 0x7fffffffLL;
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
-constexpr int kGroupM = 8;
-constexpr int kMinSkIters = 4;  // Stream-K shares shorter than this many k-tiles are not worth splitting
+using gb300::kGroupM;
 // Every workspace starts with a counter region of fixed size, so that a cached
 // workspace reused with another layout never finds partial sums where its
 // counters are: counters are zero at allocation and every call leaves them zero.
@@ -99,6 +98,7 @@ sgemm_status_t device_state(DeviceState** out, int* dev_out) {
         st.ctas_per_sm[c] = gb300::tile_kernel_prepare(TileConfig(c));
         if (st.ctas_per_sm[c] <= 0) st.init_status = SGEMM_ERR_LAUNCH;
       }
+      if (gb300::specialized_prepare() < 0) st.init_status = SGEMM_ERR_LAUNCH;
       st.tf32_ctas_per_sm = gb300::tf32_prepare();
       if (st.tf32_ctas_per_sm <= 0) st.init_status = SGEMM_ERR_LAUNCH;
       void* p = nullptr;
@@ -218,44 +218,30 @@ bool make_plan(int variant, int64_t M, int64_t N, int64_t K, const DeviceState& 
                ? g_cfg_small
                : g_cfg_large;
   const TileShape ts = gb300::tile_shape(p->cfg);
-  const int64_t tiles_m = (M + ts.bm - 1) / ts.bm, tiles_n = (N + ts.bn - 1) / ts.bn;
-  const int64_t tiles = tiles_m * tiles_n;
-  const int64_t ipt = (K + ts.bk - 1) / ts.bk;
-  if (tiles > kInt32Max || ipt > kInt32Max) return false;
-  Sched& sc = p->sc;
-  sc.tiles_m = int(tiles_m);
-  sc.tiles_n = int(tiles_n);
-  sc.group_m = kGroupM;
-  sc.iters_per_tile = int(ipt);
   const bool streamk = (variant == SGEMM_VARIANT_STREAMK || variant == SGEMM_VARIANT_STREAMK_SMALL);
   const int64_t resident = int64_t(ds.sms) * ds.ctas_per_sm[p->cfg];
-  if (!streamk || resident <= 0) {
-    sc.dp_tiles = int(tiles);
-    p->grid = int(tiles);
-    return true;
-  }
-  // Persistent: as many CTAs as fit at once.  Whole tiles fill complete
-  // waves; the tiles of the last, partial wave are shared out over K.
-  const int64_t waves = tiles / resident;
-  const int64_t rem = tiles % resident;
-  sc.dp_tiles = int(waves * resident);
-  sc.sk_tiles = int(rem);
-  p->grid = int(tiles < resident ? tiles : resident);
-  if (rem > 0) {
-    const int64_t total = rem * ipt;
-    int64_t sk_ctas = resident;
-    if (total / sk_ctas < kMinSkIters) sk_ctas = total / kMinSkIters;
-    if (sk_ctas < rem) sk_ctas = rem;  // never fewer sharers than tiles
-    if (sk_ctas > resident) sk_ctas = resident;
-    sc.sk_ctas = int(sk_ctas);
-    sc.sk_base = int(total / sk_ctas);
-    sc.sk_extra = int(total % sk_ctas);
-    p->grid = int(sc.dp_tiles > 0 ? resident : sk_ctas);
-    if (rem > kMaxSplitTiles) return false;
-    const int64_t slots = rem + sk_ctas - 1;
-    p->partial_bytes = size_t(slots) * ts.bm * ts.bn * 4;
-  }
+  const gb300::LaunchPlan lp = gb300::plan_launch(M, N, K, ts.bm, ts.bn, ts.bk, resident, streamk);
+  if (!lp.ok || lp.grid > kInt32Max) return false;
+  if (lp.sc.sk_tiles > kMaxSplitTiles) return false;
+  p->sc = lp.sc;
+  p->grid = int(lp.grid);
+  p->partial_bytes = size_t(lp.slots) * ts.bm * ts.bn * 4;
   return true;
+}
+
+// The size-specialized instance compiled for exactly this planned launch, or -1.
+int find_specialized(const Plan& p, int64_t M, int64_t N, int64_t K, const DeviceState& ds) {
+  if (p.variant != SGEMM_VARIANT_STREAMK && p.variant != SGEMM_VARIANT_STREAMK_SMALL) return -1;
+  if (int64_t(ds.sms) * ds.ctas_per_sm[p.cfg] != gb300::kSpecializedResident) return -1;
+  for (int i = 0; i < gb300::specialized_count(); ++i) {
+    const gb300::SpecShape s = gb300::specialized_shape(i);
+    if (s.cfg != p.cfg || s.m != M || s.n != N || s.k != K) continue;
+    const TileShape ts = gb300::tile_shape(p.cfg);
+    const gb300::LaunchPlan lp =
+        gb300::plan_launch(M, N, K, ts.bm, ts.bn, ts.bk, gb300::kSpecializedResident, true);
+    if (lp.ok && gb300::same_sched(lp.sc, p.sc) && lp.grid == p.grid) return i;
+  }
+  return -1;
 }
 
 // Estimated duration (microseconds) of a planned fast variant on this device.
@@ -339,7 +325,12 @@ int select_variant(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
                    int64_t ldb, const float* C, int64_t ldc, const DeviceState& ds) {
   double cost = 0.0;
   const int fast = select_fast(M, N, K, ds, &cost);
-  if (fast_path_ok(A, lda, B, ldb, C, ldc)) return fast;
+  if (fast_path_ok(A, lda, B, ldb, C, ldc)) {
+    Plan p;
+    if (make_plan(fast, M, N, K, ds, &p) && find_specialized(p, M, N, K, ds) >= 0)
+      return SGEMM_VARIANT_SPECIALIZED;
+    return fast;
+  }
   const double staged =
       cost + staging_cost_us(M, N, K, !operand_ok(A, lda), !operand_ok(B, ldb));
   return staged < guarded_cost_us(M, N, K, ds) ? SGEMM_VARIANT_STAGED : SGEMM_VARIANT_GUARDED;
@@ -431,12 +422,21 @@ sgemm_status_t run(int variant, int64_t M, int64_t N, int64_t K, float alpha, co
                : SGEMM_ERR_LAUNCH;
   }
   const bool staged = variant == SGEMM_VARIANT_STAGED;
-  if (staged)
+  const bool specialized = variant == SGEMM_VARIANT_SPECIALIZED;
+  if (staged || specialized)
     variant = select_fast(M, N, K, *ds, nullptr);
-  else if (!fast_path_ok(A, lda, B, ldb, C, ldc))
-    return SGEMM_ERR_INVALID_VALUE;
+  if (!staged && !fast_path_ok(A, lda, B, ldb, C, ldc)) return SGEMM_ERR_INVALID_VALUE;
   Plan p;
   if (!make_plan(variant, M, N, K, *ds, &p)) return SGEMM_ERR_UNSUPPORTED;
+  // The compiled-in schedule serves the plain epilogue only; the selector
+  // names it for any shape it fits, so alpha / beta fall back to the generic
+  // instance of the same schedule.
+  int spec = -1;
+  if (specialized) {
+    spec = find_specialized(p, M, N, K, *ds);
+    if (spec < 0) return SGEMM_ERR_UNSUPPORTED;
+    if (scaled) spec = -1;
+  }
   const TileShape ts = gb300::tile_shape(p.cfg);
   const Staging sg =
       make_staging(p, M, N, K, staged && !operand_ok(A, lda), staged && !operand_ok(B, ldb));
@@ -482,9 +482,10 @@ sgemm_status_t run(int variant, int64_t M, int64_t N, int64_t K, float alpha, co
   args.alpha = alpha;
   args.beta = beta;
   args.c_scalar = operand_ok(C, ldc) ? 0 : 1;
-  return gb300::launch_tile_kernel(p.cfg, tmap_a, tmap_b, args, p.sc, p.grid, stream) == cudaSuccess
-             ? SGEMM_OK
-             : SGEMM_ERR_LAUNCH;
+  const cudaError_t e =
+      spec >= 0 ? gb300::launch_specialized(spec, tmap_a, tmap_b, args, p.sc, p.grid, stream)
+                : gb300::launch_tile_kernel(p.cfg, tmap_a, tmap_b, args, p.sc, p.grid, stream);
+  return e == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
 }
 
 }  // namespace
@@ -531,7 +532,7 @@ size_t sgemm_workspace_size(int variant, int64_t M, int64_t N, int64_t K) {
     variant = select_variant(M, N, K, p, (K + 3) / 4 * 4, p, (N + 3) / 4 * 4, p, (N + 3) / 4 * 4, *ds);
   }
   const bool staged = variant == SGEMM_VARIANT_STAGED;
-  if (staged) variant = select_fast(M, N, K, *ds, nullptr);
+  if (staged || variant == SGEMM_VARIANT_SPECIALIZED) variant = select_fast(M, N, K, *ds, nullptr);
   Plan p;
   if (!make_plan(variant, M, N, K, *ds, &p)) return 0;
   // The staged variant is sized for copies of both A and B.
@@ -650,6 +651,7 @@ const char* sgemm_variant_name(int v) {
     case SGEMM_VARIANT_TILED_SMALL: return "tiled_small";
     case SGEMM_VARIANT_STREAMK_SMALL: return "streamk_small";
     case SGEMM_VARIANT_STAGED: return "staged";
+    case SGEMM_VARIANT_SPECIALIZED: return "specialized";
   }
   return "unknown";
 }

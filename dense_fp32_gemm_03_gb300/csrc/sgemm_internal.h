@@ -37,6 +37,66 @@ struct Sched {
   int32_t sk_base, sk_extra;
 };
 
+__host__ __device__ constexpr bool same_sched(const Sched& a, const Sched& b) {
+  return a.tiles_m == b.tiles_m && a.tiles_n == b.tiles_n && a.group_m == b.group_m &&
+         a.iters_per_tile == b.iters_per_tile && a.dp_tiles == b.dp_tiles &&
+         a.sk_tiles == b.sk_tiles && a.sk_ctas == b.sk_ctas && a.sk_base == b.sk_base &&
+         a.sk_extra == b.sk_extra;
+}
+
+// Constants of the work decomposition, shared by the host planner and the
+// size-specialized kernel instances (which compile the plan in).
+constexpr int kGroupM = 8;      // tile rows per raster group
+constexpr int kMinSkIters = 4;  // Stream-K shares shorter than this many k-tiles are not worth splitting
+
+struct LaunchPlan {
+  bool ok;        // false: a size does not fit the schedule's 32-bit fields
+  Sched sc;
+  int64_t grid;   // CTAs launched
+  int64_t slots;  // partial-tile slots the split tiles need (0: none)
+};
+
+// The schedule of one launch over BM x BN x BK tiles.  One tile per CTA, or
+// (streamk) a persistent grid of `resident` CTAs: whole tiles fill complete
+// waves and the tiles of the last, partial wave are shared out over K.
+__host__ __device__ constexpr LaunchPlan plan_launch(int64_t M, int64_t N, int64_t K, int bm,
+                                                     int bn, int bk, int64_t resident,
+                                                     bool streamk) {
+  LaunchPlan p{};
+  const int64_t tiles_m = (M + bm - 1) / bm, tiles_n = (N + bn - 1) / bn;
+  const int64_t tiles = tiles_m * tiles_n;
+  const int64_t ipt = (K + bk - 1) / bk;
+  p.ok = tiles <= 0x7fffffffLL && ipt <= 0x7fffffffLL;
+  if (!p.ok) return p;
+  p.sc.tiles_m = int32_t(tiles_m);
+  p.sc.tiles_n = int32_t(tiles_n);
+  p.sc.group_m = kGroupM;
+  p.sc.iters_per_tile = int32_t(ipt);
+  if (!streamk || resident <= 0) {
+    p.sc.dp_tiles = int32_t(tiles);
+    p.grid = tiles;
+    return p;
+  }
+  const int64_t waves = tiles / resident;
+  const int64_t rem = tiles % resident;
+  p.sc.dp_tiles = int32_t(waves * resident);
+  p.sc.sk_tiles = int32_t(rem);
+  p.grid = tiles < resident ? tiles : resident;
+  if (rem > 0) {
+    const int64_t total = rem * ipt;
+    int64_t sk_ctas = resident;
+    if (total / sk_ctas < kMinSkIters) sk_ctas = total / kMinSkIters;
+    if (sk_ctas < rem) sk_ctas = rem;  // never fewer sharers than tiles
+    if (sk_ctas > resident) sk_ctas = resident;
+    p.sc.sk_ctas = int32_t(sk_ctas);
+    p.sc.sk_base = int32_t(total / sk_ctas);
+    p.sc.sk_extra = int32_t(total % sk_ctas);
+    p.grid = p.sc.dp_tiles > 0 ? resident : sk_ctas;
+    p.slots = rem + sk_ctas - 1;
+  }
+  return p;
+}
+
 struct GemmArgs {
   int32_t M, N, K;
   const float* A;
@@ -78,6 +138,22 @@ int tile_kernel_prepare(TileConfig cfg);
 // tmap_a: A as a 2-D tensor (K fastest) with box {16, a_box_rows} and the
 // 64-byte swizzle; tmap_b: B (N fastest) with box {BN, 16}, no swizzle.
 cudaError_t launch_tile_kernel(TileConfig cfg, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                               const GemmArgs& args, const Sched& sched, int grid,
+                               cudaStream_t stream);
+
+// Size-specialized instances: the plain epilogue (C = A * B, 16-byte-aligned
+// C) of one configuration with M, N, K and the Stream-K schedule of
+// kSpecializedResident CTAs compiled in as constants.
+constexpr int kSpecializedResident = 152;  // GB300: 152 SMs, one CTA each
+struct SpecShape {
+  TileConfig cfg;
+  int64_t m, n, k;
+};
+int specialized_count();
+SpecShape specialized_shape(int i);
+int specialized_prepare();  // 0, or < 0 on error
+// `sched` and `grid` must be the plan the instance was compiled with.
+cudaError_t launch_specialized(int i, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                                const GemmArgs& args, const Sched& sched, int grid,
                                cudaStream_t stream);
 

@@ -130,6 +130,14 @@ auto with_cfg(int id, F&& f) {
   }
 }
 
+// a / b for a >= 0, b > 0.  A 64-bit division is a long software sequence;
+// the positions in the Stream-K iteration stream fit 31 bits for any size
+// short of 2^31 k-tile iterations, where the 32-bit division suffices.
+__device__ __forceinline__ int64_t div_nonneg(int64_t a, int32_t b) {
+  if (a <= 0x7fffffffLL) return int64_t(uint32_t(a) / uint32_t(b));
+  return a / b;
+}
+
 // One unit of work: a tile and a range [kb, ke) of its k-tiles.
 struct Unit {
   int tile, kb, ke, t_sk;  // t_sk >= 0: index of a split (Stream-K) tile
@@ -159,7 +167,7 @@ struct WorkIter {
       return true;
     }
     if (sk_pos < sk_end) {
-      u.t_sk = int(sk_pos / sc.iters_per_tile);
+      u.t_sk = int(div_nonneg(sk_pos, sc.iters_per_tile));
       const int64_t start = int64_t(u.t_sk) * sc.iters_per_tile;
       u.kb = int(sk_pos - start);
       const int64_t left = sk_end - start;
@@ -169,26 +177,6 @@ struct WorkIter {
       return true;
     }
     return false;
-  }
-};
-
-// Walks the k-tiles of all units of one CTA in order.
-struct KCursor {
-  WorkIter w;
-  Unit u;
-  int j;
-  bool valid;
-
-  __device__ __forceinline__ void init(const Sched& sc, int cta, int ctas) {
-    w.init(sc, cta);
-    j = 0;
-    valid = w.next(sc, ctas, u);
-  }
-  __device__ __forceinline__ void advance(const Sched& sc, int ctas) {
-    if (++j >= u.ke - u.kb) {
-      j = 0;
-      valid = w.next(sc, ctas, u);
-    }
   }
 };
 
@@ -206,21 +194,60 @@ __device__ __forceinline__ void tile_coords(const Sched& sc, int tile, int& tm, 
   tn = r / rows;
 }
 
+// Walks the k-tiles of all units of one CTA in order.  The tile coordinates
+// of the current unit are computed once per unit, not per k-tile: the
+// producer issues two copies per k-tile and the divisions would otherwise
+// sit on its path every time.
+struct KCursor {
+  WorkIter w;
+  Unit u;
+  int j;
+  int tm, tn;  // tile row and column of u.tile
+  bool valid;
+
+  __device__ __forceinline__ void init(const Sched& sc, int cta, int ctas) {
+    w.init(sc, cta);
+    j = 0;
+    valid = w.next(sc, ctas, u);
+    if (valid) tile_coords(sc, u.tile, tm, tn);
+  }
+  __device__ __forceinline__ void advance(const Sched& sc, int ctas) {
+    if (++j >= u.ke - u.kb) {
+      j = 0;
+      valid = w.next(sc, ctas, u);
+      if (valid) tile_coords(sc, u.tile, tm, tn);
+    }
+  }
+};
+
 // CTA that owns iteration `i` of the Stream-K iteration stream.
 __device__ __forceinline__ int sk_owner(const Sched& sc, int64_t i) {
   const int64_t big = int64_t(sc.sk_extra) * (sc.sk_base + 1);
-  if (i < big) return int(i / (sc.sk_base + 1));
-  return sc.sk_extra + int((i - big) / sc.sk_base);
+  if (i < big) return int(div_nonneg(i, sc.sk_base + 1));
+  return sc.sk_extra + int(div_nonneg(i - big, sc.sk_base));
 }
 
 // SCALED: the general epilogue, C = alpha * acc + beta * C with C read and
 // written 4 bytes at a time when it is not 16-byte aligned row by row (a
 // separate instance, so that the plain C = A * B kernel with aligned C
 // carries neither).
-template <class T, bool SCALED>
+//
+// FM, FN, FK > 0: the size-specialized instance ("Beyond Kernel 7", the
+// size-specialized kernel behind the confirmed 4096 result): the problem
+// shape and the Stream-K schedule of kSpecializedResident CTAs are compile-
+// time constants, so tile coordinates, shares and bounds fold into the code.
+// The launch must pass exactly that schedule (the host checks).
+template <class T, bool SCALED, int FM = 0, int FN = 0, int FK = 0>
 __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
     tile_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                const GemmArgs args, const Sched sc) {
+                const GemmArgs args, const Sched sc_in) {
+  Sched sc = sc_in;
+  if constexpr (FM > 0) {
+    constexpr LaunchPlan kPlan =
+        plan_launch(FM, FN, FK, T::BM, T::BN, T::BK, kSpecializedResident, true);
+    static_assert(kPlan.ok && kPlan.grid == kSpecializedResident, "specialized schedule");
+    sc = kPlan.sc;
+  }
   extern __shared__ __align__(1024) unsigned char smem[];
   float* sB = reinterpret_cast<float*>(smem + T::kBOff);
   float* sAst = reinterpret_cast<float*>(smem + T::kAStagingOff);
@@ -269,26 +296,17 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
     KCursor issue, proc;
     issue.init(sc, cta, ctas);
     proc.init(sc, cta, ctas);
-    auto tile_mn = [&](const Unit& u, int& m0, int& n0) {
-      int tm, tn;
-      tile_coords(sc, u.tile, tm, tn);
-      m0 = tm * T::BM;
-      n0 = tn * T::BN;
-    };
     auto issue_a = [&](uint32_t slot) {
-      int m0, n0;
-      tile_mn(issue.u, m0, n0);
       dev::mbar_arrive_expect_tx(&my_astage[slot], T::kAStagingBytes);
       dev::tma_load_2d(my_staging + slot * T::kAStagingFloats, &tmap_a,
-                       (issue.u.kb + issue.j) * T::BK, m0 + pw * T::kRowsPerProducer,
+                       (issue.u.kb + issue.j) * T::BK, issue.tm * T::BM + pw * T::kRowsPerProducer,
                        &my_astage[slot]);
     };
     // The B tile of k-tile `c.j` of unit `c.u` into ring stage s.
     auto issue_b = [&](const KCursor& c, uint32_t s) {
-      int m0, n0;
-      tile_mn(c.u, m0, n0);
       dev::mbar_expect_tx(&full[s], T::kBStageBytes);
-      dev::tma_load_2d(sB + s * T::kBStageFloats, &tmap_b, n0, (c.u.kb + c.j) * T::BK, &full[s]);
+      dev::tma_load_2d(sB + s * T::kBStageFloats, &tmap_b, c.tn * T::BN, (c.u.kb + c.j) * T::BK,
+                       &full[s]);
     };
     // Prologue: this warp's first S2 A slices into its staging ring and, from
     // warp 0, the B tiles of the same k-tiles (their ring stages start empty),
@@ -363,7 +381,7 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
   const int wm = warp % T::kWarpsM, wn = warp / T::kWarpsM;
   const int a_frag = wm * T::kWarpM + 4 * tr;  // + 16 g + kAStride kk
   const int b_frag = wn * T::kWarpN + 4 * tc;      // + 32 h + BN kk
-  const int M = args.M, N = args.N;
+  const int M = FM > 0 ? FM : args.M, N = FN > 0 ? FN : args.N;
 
   WorkIter w;
   w.init(sc, cta);
@@ -604,6 +622,12 @@ int prepare() {
   return blocks;
 }
 
+// The size-specialized instances: configuration id, M, N, K.
+using Spec4096 = Cfg0;  // configuration 0, the default for large shapes
+using Spec1024 = Cfg3;  // configuration 3, the default for small shapes
+constexpr SpecShape kSpecShapes[] = {{0, 4096, 4096, 4096}, {3, 1024, 1024, 1024}};
+constexpr int kSpecCount = int(sizeof(kSpecShapes) / sizeof(kSpecShapes[0]));
+
 template <class T>
 TileShape shape_of() {
   return TileShape{T::BM, T::BN, T::BK, T::NT, T::S, T::kSmem, T::kRowsPerProducer, T::kTN,
@@ -618,6 +642,39 @@ TileShape tile_shape(TileConfig cfg) {
 
 int tile_kernel_prepare(TileConfig cfg) {
   return with_cfg(cfg, [](auto c) { return prepare<decltype(c)>(); });
+}
+
+int specialized_count() { return kSpecCount; }
+
+SpecShape specialized_shape(int i) { return kSpecShapes[i]; }
+
+int specialized_prepare() {
+  if (cudaFuncSetAttribute(tile_kernel<Spec4096, false, 4096, 4096, 4096>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(Spec4096::kSmem)) != cudaSuccess ||
+      cudaFuncSetAttribute(tile_kernel<Spec1024, false, 1024, 1024, 1024>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(Spec1024::kSmem)) != cudaSuccess)
+    return -1;
+  return 0;
+}
+
+cudaError_t launch_specialized(int i, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                               const GemmArgs& args, const Sched& sched, int grid,
+                               cudaStream_t stream) {
+  switch (i) {
+    case 0:
+      tile_kernel<Spec4096, false, 4096, 4096, 4096>
+          <<<grid, Spec4096::NT, Spec4096::kSmem, stream>>>(tmap_a, tmap_b, args, sched);
+      break;
+    case 1:
+      tile_kernel<Spec1024, false, 1024, 1024, 1024>
+          <<<grid, Spec1024::NT, Spec1024::kSmem, stream>>>(tmap_a, tmap_b, args, sched);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
 }
 
 cudaError_t launch_tile_kernel(TileConfig cfg, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,

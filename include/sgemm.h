@@ -61,7 +61,8 @@ typedef enum {
   SGEMM_VARIANT_TILED_SMALL = 3,   /* pipelined 128x128 tiles, one output tile per CTA */
   SGEMM_VARIANT_STREAMK_SMALL = 4, /* Stream-K schedule over 128x128 tiles */
   SGEMM_VARIANT_STAGED = 5,    /* any stride and alignment: unaligned A, B copied aligned first */
-  SGEMM_VARIANT_COUNT = 6
+  SGEMM_VARIANT_SPECIALIZED = 6, /* Stream-K compiled for one exact shape (1024^3, 4096^3) */
+  SGEMM_VARIANT_COUNT = 7
 } sgemm_variant_t;
 
 /*
@@ -109,6 +110,16 @@ sgemm_status_t sgemm_ex(int layout, int64_t M, int64_t N, int64_t K, float alpha
  * launching.  GUARDED and STAGED take any operands; STAGED copies only the
  * operands that need it, into the per-(device, stream) workspace, and then
  * runs the pipelined schedule the selector picks for the shape.
+ *
+ * SPECIALIZED is the size-specialized form of the pipelined kernel ("Beyond
+ * Kernel 7", the size-specialized kernel of the confirmed 4096 result): the
+ * instance with M, N, K and the Stream-K schedule compiled in as constants,
+ * built for M = N = K = 1024 and M = N = K = 4096 on a 152-SM GB300.  It
+ * computes exactly what the generic Stream-K variant of the same schedule
+ * computes (bit for bit).  The selector takes it whenever the shape, the
+ * device and aligned operands allow.  Forced with operands the pipelined
+ * variants cannot take it returns SGEMM_ERR_INVALID_VALUE, on any other shape
+ * or device SGEMM_ERR_UNSUPPORTED, without launching.
  */
 sgemm_status_t sgemm_variant(int variant, int64_t M, int64_t N, int64_t K, const float *A,
                              int64_t lda, const float *B, int64_t ldb, float *C, int64_t ldc,
