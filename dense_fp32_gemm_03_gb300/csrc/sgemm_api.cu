@@ -556,19 +556,27 @@ sgemm_status_t sgemm_tf32(int64_t M, int64_t N, int64_t K, const float* A, int64
   const int64_t tiles = ((M + gb300::tf32_tile_m() - 1) / gb300::tf32_tile_m()) *
                         ((N + gb300::tf32_tile_n() - 1) / gb300::tf32_tile_n());
   if (tiles > kInt32Max) return SGEMM_ERR_UNSUPPORTED;
-  // B^T (N x K, rows padded to a multiple of 4 floats) lives in the workspace,
-  // after the counter region the Stream-K schedule relies on.
-  const int64_t ldbt = (K + 3) / 4 * 4;
-  void* ws = nullptr;
-  st = get_workspace_bytes(dev, stream, kCounterBytes + size_t(N) * size_t(ldbt) * 4, &ws);
-  if (st != SGEMM_OK) return st;
-  float* Bt = reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes);
-  if (gb300::launch_transpose(B, ldb, Bt, ldbt, int(K), int(N), stream) != cudaSuccess)
-    return SGEMM_ERR_LAUNCH;
+  // B is read in place as an MN-major operand when TMA can address it;
+  // otherwise B^T (N x K, rows padded to a multiple of 4 floats) is written to
+  // the workspace, after the counter region the Stream-K schedule relies on,
+  // and read K-major like A.
+  const bool b_mn = operand_ok(B, ldb);
+  const float* b_src = B;
+  if (!b_mn) {
+    const int64_t ldbt = (K + 3) / 4 * 4;
+    void* ws = nullptr;
+    st = get_workspace_bytes(dev, stream, kCounterBytes + size_t(N) * size_t(ldbt) * 4, &ws);
+    if (st != SGEMM_OK) return st;
+    float* Bt = reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes);
+    if (gb300::launch_transpose(B, ldb, Bt, ldbt, int(K), int(N), stream) != cudaSuccess)
+      return SGEMM_ERR_LAUNCH;
+    b_src = Bt;
+    ldb = ldbt;
+  }
 
-  CUtensorMap tmap_a, tmap_bt;
+  CUtensorMap tmap_a, tmap_b;
   std::memset(&tmap_a, 0, sizeof(tmap_a));
-  std::memset(&tmap_bt, 0, sizeof(tmap_bt));
+  std::memset(&tmap_b, 0, sizeof(tmap_b));
   const cuuint32_t estr[2] = {1, 1};
   {
     const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(M)};
@@ -580,15 +588,22 @@ sgemm_status_t sgemm_tf32(int64_t M, int64_t N, int64_t K, const float* A, int64
       return SGEMM_ERR_LAUNCH;
   }
   {
-    const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(N)};
-    const cuuint64_t strides[1] = {cuuint64_t(ldbt) * 4};
-    const cuuint32_t box[2] = {cuuint32_t(gb300::tf32_tile_k()), cuuint32_t(gb300::tf32_tile_n())};
-    if (g_encode(&tmap_bt, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, Bt, dims, strides, box, estr,
-                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    // In place: B (N fastest), boxes of 32 columns x 32 rows of k, 128-byte
+    // swizzle of 32-byte atoms (what MN-major TF32 operands take).
+    // Transposed: Bt (K fastest), boxes of 32 k x 256 rows, 128-byte swizzle.
+    const cuuint64_t dims[2] = {b_mn ? cuuint64_t(N) : cuuint64_t(K),
+                                b_mn ? cuuint64_t(K) : cuuint64_t(N)};
+    const cuuint64_t strides[1] = {cuuint64_t(ldb) * 4};
+    const cuuint32_t box[2] = {
+        b_mn ? cuuint32_t(gb300::tf32_b_chunk()) : cuuint32_t(gb300::tf32_tile_k()),
+        b_mn ? cuuint32_t(gb300::tf32_tile_k()) : cuuint32_t(gb300::tf32_tile_n())};
+    if (g_encode(&tmap_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(b_src), dims,
+                 strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 b_mn ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return SGEMM_ERR_LAUNCH;
   }
-  return gb300::launch_tf32_kernel(tmap_a, tmap_bt, int(M), int(N), int(K), C, ldc, kGroupM,
+  return gb300::launch_tf32_kernel(b_mn, tmap_a, tmap_b, int(M), int(N), int(K), C, ldc, kGroupM,
                                    ds->status, kDefaultWaitLimitNs, stream) == cudaSuccess
              ? SGEMM_OK
              : SGEMM_ERR_LAUNCH;

@@ -166,11 +166,13 @@ int tf32_prepare();  // resident CTAs per SM, or < 0 on error
 // Bt (N x K, row stride ldbt, K contiguous) = B^T.
 cudaError_t launch_transpose(const float* B, int64_t ldb, float* Bt, int64_t ldbt, int K, int N,
                              cudaStream_t stream);
-// tmap_a: A (K fastest), box {32, 128}; tmap_bt: Bt (K fastest), box {32, 256}; both with the
+int tf32_b_chunk();  // columns of B per TMA box when B is read in place (MN-major)
+// tmap_a: A (K fastest), box {32, 128}, 128-byte swizzle.  b_mn: tmap_b is B itself (N
+// fastest), box {32, 32}, 128-byte swizzle; otherwise tmap_b is Bt (K fastest), box {32, 256},
 // 128-byte swizzle.
-cudaError_t launch_tf32_kernel(const CUtensorMap& tmap_a, const CUtensorMap& tmap_bt, int M, int N,
-                               int K, float* C, int64_t ldc, int group_m, uint32_t* status,
-                               uint64_t limit, cudaStream_t stream);
+cudaError_t launch_tf32_kernel(bool b_mn, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                               int M, int N, int K, float* C, int64_t ldc, int group_m,
+                               uint32_t* status, uint64_t limit, cudaStream_t stream);
 
 cudaError_t launch_guarded_kernel(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
                                   const float* B, int64_t ldb, float* C, int64_t ldc, int scaled,

@@ -9,11 +9,16 @@
 // FP32 FFMA path.
 //
 // Structure (one output tile of 128 x 256 per CTA):
-//  * B is first rewritten K-major (transpose_kernel) so that both operands
-//    reach shared memory by TMA already in the canonical K-major layout with
-//    the 128-byte swizzle that tcgen05.mma reads through its shared-memory
-//    descriptors.
-//  * warp 0 (one lane) streams 32-deep k-slices of A (128 x 32) and B^T
+//  * A reaches shared memory by TMA in the canonical K-major layout with the
+//    128-byte swizzle that tcgen05.mma reads through its shared-memory
+//    descriptors.  B, row-major (N contiguous), is read as an MN-major
+//    operand: a 32-deep k-slice of its 256 columns arrives as eight 32 x 32
+//    boxes (128 bytes of N by 32 rows of k, 128-byte swizzle of 32-byte
+//    atoms) 4 KB apart.
+//    Only a B that TMA cannot read in place (a misaligned base or a row
+//    stride that is not a multiple of 4) is first rewritten K-major
+//    (transpose_kernel) and read like A.
+//  * warp 0 (one lane) streams 32-deep k-slices of A (128 x 32) and B
 //    (256 x 32) into a 4-stage ring (full / empty mbarriers);
 //  * warp 1 allocates 256 TMEM columns and one lane issues
 //    tcgen05.mma.cta_group::1.kind::tf32 (M = 128, N = 256, K = 8, four per
@@ -38,12 +43,18 @@ constexpr size_t kTfSmem = 1024 /* alignment slack */ + kTfStages * size_t(kTfAS
 constexpr uint32_t kStatusTimeout = 3;
 
 // Instruction descriptor of tcgen05.mma kind::tf32: FP32 accumulator, TF32 A
-// and B, both K-major, M = 128, N = 256.
-constexpr uint32_t kTfIdesc = (1u << 4)                 // D format: F32
-                              | (2u << 7)               // A format: TF32
-                              | (2u << 10)              // B format: TF32
-                              | (0u << 15) | (0u << 16) // A, B K-major
-                              | (uint32_t(kTfBN >> 3) << 17) | (uint32_t(kTfBM >> 4) << 24);
+// and B, A K-major, B K-major (b_mn = 0) or MN-major (b_mn = 1), M = 128,
+// N = 256.
+__host__ __device__ constexpr uint32_t tf_idesc(uint32_t b_mn) {
+  return (1u << 4)                  // D format: F32
+         | (2u << 7)                // A format: TF32
+         | (2u << 10)               // B format: TF32
+         | (0u << 15) | (b_mn << 16)  // A K-major; B K- or MN-major
+         | (uint32_t(kTfBN >> 3) << 17) | (uint32_t(kTfBM >> 4) << 24);
+}
+// B as an MN-major operand: 32-column (128-byte) chunks of N, one TMA box each.
+constexpr int kTfBChunk = 32;
+constexpr uint32_t kTfBChunkBytes = kTfBChunk * kTfBK * 4;  // 4 KB: 32 rows of k x 128 bytes
 
 // Shared-memory matrix descriptor for a K-major operand stored as rows of 128
 // bytes with the 128-byte swizzle: 8-row core groups 1024 bytes apart.
@@ -57,13 +68,33 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
   return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major TF32 operand stored as
+// 128-byte (32-element) chunks of MN, each chunk 32 rows of k, with the
+// 128-byte swizzle of 32-byte atoms (TMA's SWIZZLE_128B_ATOM_32B; 4-row
+// period).  TF32 in MN-major form takes this swizzle: with the plain 128-byte
+// one the tensor core produced zeros on GB300.  The leading byte offset steps
+// to the next MN chunk (4 KB), the stride byte offset to the next 4-row group
+// of k (512 bytes), so one K = 8 instruction reads two groups.  Established
+// on GB300 by multiplying A[m][k] = (k == m mod 8) with B[k][n] = 256 k + n,
+// which shows which B element meets each (k, n).
+__device__ __forceinline__ uint64_t sw128a32_mnmajor_desc(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= uint64_t((smem_addr & 0x3FFFFu) >> 4);  // start address
+  d |= uint64_t(kTfBChunkBytes >> 4) << 16;    // leading byte offset: next MN chunk
+  d |= uint64_t(512 >> 4) << 32;               // stride byte offset: next 4 rows of k
+  d |= uint64_t(1) << 46;                      // descriptor version for sm_100 family
+  d |= uint64_t(1) << 61;                      // layout: 128-byte swizzle, 32-byte atoms
+  return d;
+}
+
+template <uint32_t kIdesc>
 __device__ __forceinline__ void tc_mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                             uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(kTfIdesc), "r"(accumulate)
+      "l"(a_desc), "l"(b_desc), "n"(kIdesc), "r"(accumulate)
       : "memory");
 }
 
@@ -87,6 +118,9 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// B_MN: B is read in place as an MN-major operand (tmap_b: B, N fastest, box
+// 32 x 32); otherwise tmap_b holds B^T (K fastest, box 32 x 256) like A.
+template <bool B_MN>
 __global__ void __launch_bounds__(kTfThreads, 1)
     tf32_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_bt,
                 int M, int N, int K, float* __restrict__ C, int64_t ldc, int tiles_m, int tiles_n,
@@ -153,7 +187,14 @@ __global__ void __launch_bounds__(kTfThreads, 1)
         if (*s_abort) break;
         dev::mbar_arrive_expect_tx(&full[s], kTfAStageBytes + kTfBStageBytes);
         dev::tma_load_2d(sA + s * kTfAStageBytes, &tmap_a, kt * kTfBK, m0, &full[s]);
-        dev::tma_load_2d(sB + s * kTfBStageBytes, &tmap_bt, kt * kTfBK, n0, &full[s]);
+        if constexpr (B_MN) {
+#pragma unroll
+          for (int j = 0; j < kTfBN / kTfBChunk; ++j)
+            dev::tma_load_2d(sB + s * kTfBStageBytes + j * kTfBChunkBytes, &tmap_bt,
+                             n0 + j * kTfBChunk, kt * kTfBK, &full[s]);
+        } else {
+          dev::tma_load_2d(sB + s * kTfBStageBytes, &tmap_bt, kt * kTfBK, n0, &full[s]);
+        }
       }
     }
   } else if (warp == 1) {
@@ -167,10 +208,16 @@ __global__ void __launch_bounds__(kTfThreads, 1)
         }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint64_t a_desc = sw128_kmajor_desc(dev::smem_addr(sA + s * kTfAStageBytes));
-        const uint64_t b_desc = sw128_kmajor_desc(dev::smem_addr(sB + s * kTfBStageBytes));
+        const uint32_t b_addr = dev::smem_addr(sB + s * kTfBStageBytes);
+        const uint64_t b_desc = B_MN ? sw128a32_mnmajor_desc(b_addr) : sw128_kmajor_desc(b_addr);
+        // K = 8 TF32 per instruction: 32 bytes along a K-major row, or 8 rows
+        // (1 KB) of an MN-major chunk.  Descriptor addresses are in 16-byte
+        // units.
+        constexpr uint64_t kBStep = B_MN ? 1024 / 16 : 32 / 16;
 #pragma unroll
-        for (int k = 0; k < kTfBK / 8; ++k)  // K = 8 TF32 = 32 bytes per instruction
-          tc_mma_tf32(tmem, a_desc + 2 * k, b_desc + 2 * k, (kt | k) != 0 ? 1u : 0u);
+        for (int k = 0; k < kTfBK / 8; ++k)
+          tc_mma_tf32<tf_idesc(B_MN ? 1u : 0u)>(tmem, a_desc + 2 * k, b_desc + kBStep * k,
+                                                (kt | k) != 0 ? 1u : 0u);
         tc_commit(&empty[s]);  // the stage is free once these MMAs have read it
       }
       tc_commit(accum);  // the accumulator is final once every MMA completed
@@ -288,13 +335,17 @@ int tf32_tile_m() { return kTfBM; }
 int tf32_tile_n() { return kTfBN; }
 int tf32_tile_k() { return kTfBK; }
 
+int tf32_b_chunk() { return kTfBChunk; }
+
 int tf32_prepare() {
-  if (cudaFuncSetAttribute(tf32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kTfSmem)) !=
-      cudaSuccess)
+  if (cudaFuncSetAttribute(tf32_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(kTfSmem)) != cudaSuccess ||
+      cudaFuncSetAttribute(tf32_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(kTfSmem)) != cudaSuccess)
     return -1;
   int blocks = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, tf32_kernel, kTfThreads, kTfSmem) !=
-      cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, tf32_kernel<true>, kTfThreads,
+                                                    kTfSmem) != cudaSuccess)
     return -1;
   return blocks;
 }
@@ -315,12 +366,16 @@ cudaError_t launch_transpose(const float* B, int64_t ldb, float* Bt, int64_t ldb
   return cudaGetLastError();
 }
 
-cudaError_t launch_tf32_kernel(const CUtensorMap& tmap_a, const CUtensorMap& tmap_bt, int M, int N,
-                               int K, float* C, int64_t ldc, int group_m, uint32_t* status,
-                               uint64_t limit, cudaStream_t stream) {
+cudaError_t launch_tf32_kernel(bool b_mn, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                               int M, int N, int K, float* C, int64_t ldc, int group_m,
+                               uint32_t* status, uint64_t limit, cudaStream_t stream) {
   const int tiles_m = (M + kTfBM - 1) / kTfBM, tiles_n = (N + kTfBN - 1) / kTfBN;
-  tf32_kernel<<<tiles_m * tiles_n, kTfThreads, kTfSmem, stream>>>(
-      tmap_a, tmap_bt, M, N, K, C, ldc, tiles_m, tiles_n, group_m, status, limit);
+  if (b_mn)
+    tf32_kernel<true><<<tiles_m * tiles_n, kTfThreads, kTfSmem, stream>>>(
+        tmap_a, tmap_b, M, N, K, C, ldc, tiles_m, tiles_n, group_m, status, limit);
+  else
+    tf32_kernel<false><<<tiles_m * tiles_n, kTfThreads, kTfSmem, stream>>>(
+        tmap_a, tmap_b, M, N, K, C, ldc, tiles_m, tiles_n, group_m, status, limit);
   return cudaGetLastError();
 }
 

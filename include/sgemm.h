@@ -154,7 +154,8 @@ size_t sgemm_workspace_size(int variant, int64_t M, int64_t N, int64_t K);
  *
  * Same arguments and ownership as sgemm().  A and C must be 16-byte aligned
  * with lda and ldc multiples of 4 (else SGEMM_ERR_INVALID_VALUE); B may have
- * any stride.  B is first copied transposed into the per-(device, stream)
+ * any stride.  A 16-byte-aligned B with ldb a multiple of 4 is read in place;
+ * any other B is first copied transposed into the per-(device, stream)
  * workspace (N * round_up(K, 4) floats), which may grow with cudaMalloc as
  * for sgemm().
  */

@@ -109,3 +109,45 @@ def test_tf32_rejects_misaligned_a():
     B = torch.ones(65, 64, device="cuda")
     with pytest.raises(sg.SgemmError):
         sg.sgemm_tf32(A, B)
+
+
+@pytest.mark.parametrize("shape", [(256, 256, 256), (384, 520, 96), (129, 300, 77), (300, 33, 1029)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_tf32_b_in_place_and_transposed(shape):
+    """B read in place (MN-major, 16-byte aligned rows) and B copied transposed first
+    (a base 4 bytes off alignment) give results within the bound, on every tile edge."""
+    M, N, K = shape
+    lda = (K + 3) // 4 * 4
+    A = workloads.matrix(M, K, "uniform", 90 + M, 0)
+    B = workloads.matrix(K, N, "uniform", 90 + M, 1)
+    ref, E = oracle.sgemm_f64(A, B)
+    A_dev = torch.zeros(M, lda, device="cuda")
+    A_dev[:, :K] = A.cuda()
+    A_dev = A_dev[:, :K]
+    ldb = (N + 3) // 4 * 4
+    B_aligned = torch.zeros(K, ldb, device="cuda")
+    B_aligned[:, :N] = B.cuda()
+    B_aligned = B_aligned[:, :N]
+    flat = torch.zeros(K * N + 1, device="cuda")
+    B_offset = flat[1:].view(K, N)
+    B_offset.copy_(B.cuda())
+    ldc = (N + 3) // 4 * 4                       # C's row stride must be a multiple of 4
+    for what, Bd in (("in place", B_aligned), ("transposed", B_offset)):
+        C = torch.full((M, ldc), float("nan"), device="cuda")[:, :N]
+        sg.sgemm_tf32(A_dev, Bd, out=C)
+        torch.cuda.synchronize()
+        check_tf32(C.cpu().numpy(), ref, E, K, f"tf32 {shape} B {what}")
+
+
+def test_tf32_integers_exact_through_both_b_paths():
+    M, N, K = 256, 512, 384
+    A = workloads.matrix(M, K, "int8range", 95, 0)
+    B = workloads.matrix(K, N, "int8range", 95, 1)
+    ref, _ = oracle.sgemm_f64(A, B)
+    flat = torch.zeros(K * N + 3, device="cuda")
+    B_offset = flat[3:].view(K, N)
+    B_offset.copy_(B.cuda())
+    for Bd in (B.cuda(), B_offset):
+        C = sg.sgemm_tf32(A.cuda(), Bd)
+        torch.cuda.synchronize()
+        check_exact(C.cpu().numpy(), ref, "tf32 integers")
