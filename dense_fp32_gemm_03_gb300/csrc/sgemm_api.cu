@@ -553,21 +553,34 @@ sgemm_status_t sgemm_tf32(int64_t M, int64_t N, int64_t K, const float* A, int64
   }
   // A goes to the tensor cores by TMA and C is stored 128 bits at a time.
   if (!aligned16(A) || !aligned16(C) || lda % 4 != 0 || ldc % 4 != 0) return SGEMM_ERR_INVALID_VALUE;
-  const int64_t tiles = ((M + gb300::tf32_tile_m() - 1) / gb300::tf32_tile_m()) *
-                        ((N + gb300::tf32_tile_n() - 1) / gb300::tf32_tile_n());
-  if (tiles > kInt32Max) return SGEMM_ERR_UNSUPPORTED;
+  // 128 x 256 x 32 tiles.  More tiles than resident CTAs: a persistent
+  // Stream-K schedule (one CTA per SM) that splits the last partial wave over
+  // K.  At most one wave: one tile per CTA, since reducing 128 KB partial
+  // tiles then costs more than the idle SMs (measured on GB300 from 1024^3
+  // to 2048^3; from 2560^3 up the split schedule wins).
+  const int64_t resident = int64_t(ds->sms) * ds->tf32_ctas_per_sm;
+  const int bm = gb300::tf32_tile_m(), bn = gb300::tf32_tile_n(), bk = gb300::tf32_tile_k();
+  const int64_t tiles = ((M + bm - 1) / bm) * ((N + bn - 1) / bn);
+  const gb300::LaunchPlan lp = gb300::plan_launch(M, N, K, bm, bn, bk, resident, tiles > resident);
+  if (!lp.ok || lp.grid > kInt32Max || lp.sc.sk_tiles > kMaxSplitTiles)
+    return SGEMM_ERR_UNSUPPORTED;
+  // Workspace: [counters][partial slots][B^T when B cannot be read in place].
+  const size_t slot_bytes = size_t(gb300::tf32_tile_m()) * gb300::tf32_tile_n() * 4;
+  const size_t partial_bytes = size_t(lp.slots) * slot_bytes;
   // B is read in place as an MN-major operand when TMA can address it;
-  // otherwise B^T (N x K, rows padded to a multiple of 4 floats) is written to
-  // the workspace, after the counter region the Stream-K schedule relies on,
-  // and read K-major like A.
+  // otherwise B^T (N x K, rows padded to a multiple of 4 floats) is written
+  // to the workspace and read K-major like A.
   const bool b_mn = operand_ok(B, ldb);
+  const int64_t ldbt = (K + 3) / 4 * 4;
+  const size_t bt_off = kCounterBytes + round_up(partial_bytes, 256);
+  const size_t ws_bytes =
+      b_mn ? (partial_bytes ? kCounterBytes + partial_bytes : 0) : bt_off + size_t(N) * ldbt * 4;
+  void* ws = nullptr;
+  st = get_workspace_bytes(dev, stream, ws_bytes, &ws);
+  if (st != SGEMM_OK) return st;
   const float* b_src = B;
   if (!b_mn) {
-    const int64_t ldbt = (K + 3) / 4 * 4;
-    void* ws = nullptr;
-    st = get_workspace_bytes(dev, stream, kCounterBytes + size_t(N) * size_t(ldbt) * 4, &ws);
-    if (st != SGEMM_OK) return st;
-    float* Bt = reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes);
+    float* Bt = reinterpret_cast<float*>(static_cast<char*>(ws) + bt_off);
     if (gb300::launch_transpose(B, ldb, Bt, ldbt, int(K), int(N), stream) != cudaSuccess)
       return SGEMM_ERR_LAUNCH;
     b_src = Bt;
@@ -603,8 +616,17 @@ sgemm_status_t sgemm_tf32(int64_t M, int64_t N, int64_t K, const float* A, int64
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return SGEMM_ERR_LAUNCH;
   }
-  return gb300::launch_tf32_kernel(b_mn, tmap_a, tmap_b, int(M), int(N), int(K), C, ldc, kGroupM,
-                                   ds->status, kDefaultWaitLimitNs, stream) == cudaSuccess
+  gb300::Tf32Args args{};
+  args.M = int(M);
+  args.N = int(N);
+  args.C = C;
+  args.ldc = ldc;
+  args.counters = static_cast<int32_t*>(ws);
+  args.partials = ws ? reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes) : nullptr;
+  args.status = ds->status;
+  args.wait_limit_ns = kDefaultWaitLimitNs;
+  return gb300::launch_tf32_kernel(b_mn, tmap_a, tmap_b, args, lp.sc, int(lp.grid), stream) ==
+                 cudaSuccess
              ? SGEMM_OK
              : SGEMM_ERR_LAUNCH;
 }

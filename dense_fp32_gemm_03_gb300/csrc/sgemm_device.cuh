@@ -109,6 +109,20 @@ __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
 }
 
 // Records the first error of a launch in the device status word.
+// True in exactly one active lane of the warp (the same one while the active
+// set does not change).  A loop run by the whole warp keeps its state
+// warp-uniform; the one lane then issues the single-thread instructions
+// (TMA copies, tensor-core MMAs, commits).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // Load with acquire semantics at GPU scope: writes another CTA released
 // before storing this value are visible after it.
 __device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {

@@ -167,12 +167,22 @@ int tf32_prepare();  // resident CTAs per SM, or < 0 on error
 cudaError_t launch_transpose(const float* B, int64_t ldb, float* Bt, int64_t ldbt, int K, int N,
                              cudaStream_t stream);
 int tf32_b_chunk();  // columns of B per TMA box when B is read in place (MN-major)
+struct Tf32Args {
+  int32_t M, N;
+  float* C;
+  int64_t ldc;
+  float* partials;    // split-tile partial sums (128 x 256 floats per slot), or null
+  int32_t* counters;  // one arrival counter per split tile, zero on entry, zero on exit
+  uint32_t* status;   // device status word
+  uint64_t wait_limit_ns;
+};
 // tmap_a: A (K fastest), box {32, 128}, 128-byte swizzle.  b_mn: tmap_b is B itself (N
-// fastest), box {32, 32}, 128-byte swizzle; otherwise tmap_b is Bt (K fastest), box {32, 256},
-// 128-byte swizzle.
+// fastest), box {32, 32}, 128-byte swizzle of 32-byte atoms; otherwise tmap_b is Bt (K
+// fastest), box {32, 256}, 128-byte swizzle.  `sched` is plan_launch over 128 x 256 x 32
+// tiles for `grid` persistent CTAs.
 cudaError_t launch_tf32_kernel(bool b_mn, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
-                               int M, int N, int K, float* C, int64_t ldc, int group_m,
-                               uint32_t* status, uint64_t limit, cudaStream_t stream);
+                               const Tf32Args& args, const Sched& sched, int grid,
+                               cudaStream_t stream);
 
 cudaError_t launch_guarded_kernel(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
                                   const float* B, int64_t ldb, float* C, int64_t ldc, int scaled,

@@ -8,28 +8,33 @@
 // Kernel 7 uses mma.sync m16n8k4 TF32 on sm_120).  It never stands in for the
 // FP32 FFMA path.
 //
-// Structure (one output tile of 128 x 256 per CTA):
+// Structure: a persistent grid of one CTA per SM walks the same work
+// decomposition as the FFMA kernel (Sched: whole 128 x 256 tiles in full
+// waves, the tiles of the last partial wave split over K, Stream-K).
 //  * A reaches shared memory by TMA in the canonical K-major layout with the
 //    128-byte swizzle that tcgen05.mma reads through its shared-memory
 //    descriptors.  B, row-major (N contiguous), is read as an MN-major
 //    operand: a 32-deep k-slice of its 256 columns arrives as eight 32 x 32
 //    boxes (128 bytes of N by 32 rows of k, 128-byte swizzle of 32-byte
-//    atoms) 4 KB apart.
-//    Only a B that TMA cannot read in place (a misaligned base or a row
-//    stride that is not a multiple of 4) is first rewritten K-major
-//    (transpose_kernel) and read like A.
-//  * warp 0 (one lane) streams 32-deep k-slices of A (128 x 32) and B
+//    atoms) 4 KB apart.  Only a B that TMA cannot read in place (a
+//    misaligned base or a row stride that is not a multiple of 4) is first
+//    rewritten K-major (transpose_kernel) and read like A.
+//  * warp 0 (one lane) streams the CTA's k-slices of A (128 x 32) and B
 //    (256 x 32) into a 4-stage ring (full / empty mbarriers);
-//  * warp 1 allocates 256 TMEM columns and one lane issues
-//    tcgen05.mma.cta_group::1.kind::tf32 (M = 128, N = 256, K = 8, four per
-//    k-slice), releasing each stage with tcgen05.commit;
-//  * warps 2-5 wait for the accumulator, read it with tcgen05.ld (each warp
-//    its 32-lane quarter of TMEM, i.e. 32 rows of C) and store C.
+//  * warp 1 allocates 512 TMEM columns (two 128 x 256 FP32 accumulators) and
+//    one lane issues tcgen05.mma.cta_group::1.kind::tf32 (M = 128, N = 256,
+//    K = 8, four per k-slice) into accumulator u mod 2 for the CTA's u-th
+//    unit, releasing stages with tcgen05.commit;
+//  * warps 2-5 read each finished accumulator with tcgen05.ld (each warp its
+//    32-lane quarter, i.e. 32 rows of C) while the MMAs of the next unit run
+//    into the other one, and store C; a split tile's sharers publish their
+//    partial sums and the last to arrive adds them in CTA order.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "sgemm_device.cuh"
 #include "sgemm_internal.h"
+#include "sgemm_sched.cuh"
 
 namespace gb300 {
 namespace {
@@ -37,9 +42,12 @@ namespace {
 constexpr int kTfBM = 128, kTfBN = 256, kTfBK = 32, kTfStages = 4, kTfThreads = 192;
 constexpr uint32_t kTfAStageBytes = kTfBM * kTfBK * 4;  // 16 KB
 constexpr uint32_t kTfBStageBytes = kTfBN * kTfBK * 4;  // 32 KB
-constexpr uint32_t kTfTmemCols = 256;                   // 128 lanes x 256 FP32 columns
+constexpr uint32_t kTfTmemCols = 2 * kTfBN;             // two accumulators of 128 lanes x 256 FP32
+constexpr int kTfEpiWarps = 4;                          // warps 2..5
+constexpr int kTfEpiThreads = 32 * kTfEpiWarps;
+constexpr int kTfBarriers = 2 * kTfStages + 5;          // full, empty, acc_full[2], acc_empty[2], drain
 constexpr size_t kTfSmem = 1024 /* alignment slack */ + kTfStages * size_t(kTfAStageBytes + kTfBStageBytes) +
-                           (2 * kTfStages + 1) * 8 + 16;
+                           kTfBarriers * 8 + 16;
 constexpr uint32_t kStatusTimeout = 3;
 
 // Instruction descriptor of tcgen05.mma kind::tf32: FP32 accumulator, TF32 A
@@ -118,13 +126,28 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Stores 32 consecutive values of row `row` of C from column `col` on.
+__device__ __forceinline__ void store_row32(const Tf32Args& args, int row, int col,
+                                            const float (&v)[32]) {
+  if (row >= args.M) return;
+  float* dst = args.C + int64_t(row) * args.ldc + col;
+  if (col + 32 <= args.N) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      reinterpret_cast<float4*>(dst)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (col + i < args.N) dst[i] = v[i];
+  }
+}
+
 // B_MN: B is read in place as an MN-major operand (tmap_b: B, N fastest, box
 // 32 x 32); otherwise tmap_b holds B^T (K fastest, box 32 x 256) like A.
 template <bool B_MN>
 __global__ void __launch_bounds__(kTfThreads, 1)
-    tf32_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_bt,
-                int M, int N, int K, float* __restrict__ C, int64_t ldc, int tiles_m, int tiles_n,
-                int group_m, uint32_t* status, uint64_t limit) {
+    tf32_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                const Tf32Args args, const Sched sc) {
   extern __shared__ unsigned char smem_raw[];
   // Stages must sit on 1024-byte boundaries (the 128-byte swizzle period).
   const uint32_t raw = dev::smem_addr(smem_raw);
@@ -133,20 +156,16 @@ __global__ void __launch_bounds__(kTfThreads, 1)
   unsigned char* sB = smem + kTfStages * kTfAStageBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(sB + kTfStages * kTfBStageBytes);
   uint64_t* empty = full + kTfStages;
-  uint64_t* accum = empty + kTfStages;
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(accum + 1);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(accum + 1) + 1;
+  uint64_t* acc_full = empty + kTfStages;  // [2] accumulator b holds a finished unit
+  uint64_t* acc_empty = acc_full + 2;      // [2] the epilogue has read accumulator b
+  uint64_t* drain = acc_empty + 2;         // every MMA this CTA issued has completed
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(drain + 1);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(drain + 1) + 1;
+  int* s_last = reinterpret_cast<int*>(drain + 1) + 2;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Grouped raster over tiles, as the FFMA kernel does.
-  const int tile = blockIdx.x;
-  const int per_group = group_m * tiles_n;
-  const int g = tile / per_group;
-  const int first = g * group_m;
-  const int rows = min(tiles_m - first, group_m);
-  const int m0 = (first + (tile - g * per_group) % rows) * kTfBM;
-  const int n0 = ((tile - g * per_group) / rows) * kTfBN;
-  const int num_k = (K + kTfBK - 1) / kTfBK;
+  const int cta = blockIdx.x, ctas = gridDim.x;
+  const uint64_t limit = args.wait_limit_ns;
 
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -160,7 +179,11 @@ __global__ void __launch_bounds__(kTfThreads, 1)
       dev::mbar_init(&full[s], 1);
       dev::mbar_init(&empty[s], 1);
     }
-    dev::mbar_init(accum, 1);
+    for (int b = 0; b < 2; ++b) {
+      dev::mbar_init(&acc_full[b], 1);
+      dev::mbar_init(&acc_empty[b], kTfEpiWarps);  // one arrival per epilogue warp
+    }
+    dev::mbar_init(drain, 1);
     *s_abort = 0;
     dev::mbar_init_fence();
   }
@@ -169,86 +192,212 @@ __global__ void __launch_bounds__(kTfThreads, 1)
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
 
+  // A wait that failed: record it once and make every later wait give up at
+  // once, so that all roles run to their end without waiting.
   auto fail = [&]() {
     if (!*s_abort) {
       *s_abort = 1;
-      dev::record_status(status, kStatusTimeout, kWaitTileStage);
+      dev::record_status(args.status, kStatusTimeout, kWaitTileStage);
     }
   };
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ---- TMA producer
+    // ---- TMA producer: the CTA's k-slices, unit after unit.  The whole warp
+    // walks the schedule and waits; one elected lane issues the copies.
+    if (dev::elect_one()) {
       dev::tma_prefetch_desc(&tmap_a);
-      dev::tma_prefetch_desc(&tmap_bt);
-      for (int kt = 0; kt < num_k; ++kt) {
-        const int s = kt % kTfStages, n = kt / kTfStages;
-        if (n > 0 && !dev::mbar_wait_abortable(&empty[s], (n - 1) & 1u, limit, s_abort)) fail();
-        if (*s_abort) break;
+      dev::tma_prefetch_desc(&tmap_b);
+    }
+    KCursor c;
+    c.init(sc, cta, ctas);
+    uint32_t i = 0;
+    for (; c.valid; ++i, c.advance(sc, ctas)) {
+      const uint32_t s = i % kTfStages, n = i / kTfStages;
+      if (n > 0 && !dev::mbar_wait_abortable(&empty[s], (n - 1) & 1u, limit, s_abort)) fail();
+      if (*s_abort) break;
+      const int k0 = (c.u.kb + c.j) * kTfBK, m0 = c.tm * kTfBM, n0 = c.tn * kTfBN;
+      if (dev::elect_one()) {
         dev::mbar_arrive_expect_tx(&full[s], kTfAStageBytes + kTfBStageBytes);
-        dev::tma_load_2d(sA + s * kTfAStageBytes, &tmap_a, kt * kTfBK, m0, &full[s]);
+        dev::tma_load_2d(sA + s * kTfAStageBytes, &tmap_a, k0, m0, &full[s]);
         if constexpr (B_MN) {
 #pragma unroll
           for (int j = 0; j < kTfBN / kTfBChunk; ++j)
-            dev::tma_load_2d(sB + s * kTfBStageBytes + j * kTfBChunkBytes, &tmap_bt,
-                             n0 + j * kTfBChunk, kt * kTfBK, &full[s]);
+            dev::tma_load_2d(sB + s * kTfBStageBytes + j * kTfBChunkBytes, &tmap_b,
+                             n0 + j * kTfBChunk, k0, &full[s]);
         } else {
-          dev::tma_load_2d(sB + s * kTfBStageBytes, &tmap_bt, kt * kTfBK, n0, &full[s]);
+          dev::tma_load_2d(sB + s * kTfBStageBytes, &tmap_b, k0, n0, &full[s]);
         }
       }
+      __syncwarp();
     }
+    // After a failure, let the copies already issued land (bounded) before
+    // the CTA's shared memory is released.
+    if (*s_abort)
+      for (uint32_t k = (i > kTfStages ? i - kTfStages : 0); k < i; ++k)
+        dev::mbar_wait(&full[k % kTfStages], (k / kTfStages) & 1u, limit);
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---- MMA issuer
-      for (int kt = 0; kt < num_k; ++kt) {
-        const int s = kt % kTfStages;
-        if (!dev::mbar_wait_abortable(&full[s], (kt / kTfStages) & 1u, limit, s_abort)) {
-          fail();
-          break;
-        }
+    // ---- MMA issuer: unit u accumulates into TMEM columns [256 (u mod 2), +256).
+    // The whole warp walks the schedule and waits; one elected lane issues.
+    WorkIter w;
+    w.init(sc, cta);
+    Unit u;
+    uint32_t it = 0, ui = 0;
+    while (w.next(sc, ctas, u)) {
+      const uint32_t b = ui & 1u, nb = ui >> 1;
+      if (nb > 0 && !dev::mbar_wait_abortable(&acc_empty[b], (nb - 1) & 1u, limit, s_abort))
+        fail();
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t d = tmem + b * kTfBN;
+      const int nk = u.ke - u.kb;
+      for (int j = 0; j < nk; ++j, ++it) {
+        const uint32_t s = it % kTfStages;
+        if (!dev::mbar_wait_abortable(&full[s], (it / kTfStages) & 1u, limit, s_abort)) fail();
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint64_t a_desc = sw128_kmajor_desc(dev::smem_addr(sA + s * kTfAStageBytes));
-        const uint32_t b_addr = dev::smem_addr(sB + s * kTfBStageBytes);
-        const uint64_t b_desc = B_MN ? sw128a32_mnmajor_desc(b_addr) : sw128_kmajor_desc(b_addr);
-        // K = 8 TF32 per instruction: 32 bytes along a K-major row, or 8 rows
-        // (1 KB) of an MN-major chunk.  Descriptor addresses are in 16-byte
-        // units.
-        constexpr uint64_t kBStep = B_MN ? 1024 / 16 : 32 / 16;
+        if (dev::elect_one()) {
+          if (!*s_abort) {
+            const uint64_t a_desc = sw128_kmajor_desc(dev::smem_addr(sA + s * kTfAStageBytes));
+            const uint32_t b_addr = dev::smem_addr(sB + s * kTfBStageBytes);
+            const uint64_t b_desc =
+                B_MN ? sw128a32_mnmajor_desc(b_addr) : sw128_kmajor_desc(b_addr);
+            // K = 8 TF32 per instruction: 32 bytes along a K-major row, or 8
+            // rows (1 KB) of an MN-major chunk.  Descriptor addresses are in
+            // 16-byte units.
+            constexpr uint64_t kBStep = B_MN ? 1024 / 16 : 32 / 16;
 #pragma unroll
-        for (int k = 0; k < kTfBK / 8; ++k)
-          tc_mma_tf32<tf_idesc(B_MN ? 1u : 0u)>(tmem, a_desc + 2 * k, b_desc + kBStep * k,
-                                                (kt | k) != 0 ? 1u : 0u);
-        tc_commit(&empty[s]);  // the stage is free once these MMAs have read it
+            for (int k = 0; k < kTfBK / 8; ++k)
+              tc_mma_tf32<tf_idesc(B_MN ? 1u : 0u)>(d, a_desc + 2 * k, b_desc + kBStep * k,
+                                                    (j | k) != 0 ? 1u : 0u);
+          }
+          tc_commit(&empty[s]);  // the stage is free once these MMAs have read it
+        }
+        __syncwarp();
       }
-      tc_commit(accum);  // the accumulator is final once every MMA completed
+      if (dev::elect_one()) tc_commit(&acc_full[b]);  // the unit's accumulator is final
+      __syncwarp();
+      ++ui;
     }
+    if (dev::elect_one()) tc_commit(drain);
+    __syncwarp();
+    dev::mbar_wait(drain, 0u, limit);  // nothing of this CTA is left in the tensor pipe
   } else {
-    // ---- epilogue: warps 2..5 own TMEM lane quarters (warp % 4)
+    // ---- epilogue: warps 2..5 own TMEM lane quarters (warp % 4), 32 rows each
     const int q = warp & 3;
-    if (!dev::mbar_wait_abortable(accum, 0u, limit, s_abort)) fail();
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    const int row = m0 + 32 * q + lane;
+    const int row_local = 32 * q + lane;
+    const int etid = threadIdx.x - 64;  // 0..127
+    constexpr int64_t kSlotVec = int64_t(kTfBM) * kTfBN / 4;
+    WorkIter w;
+    w.init(sc, cta);
+    Unit u;
+    uint32_t ui = 0;
+    while (w.next(sc, ctas, u)) {
+      const uint32_t b = ui & 1u, nb = ui >> 1;
+      if (!dev::mbar_wait_abortable(&acc_full[b], nb & 1u, limit, s_abort)) fail();
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      int tm, tn;
+      tile_coords(sc, u.tile, tm, tn);
+      const int row = tm * kTfBM + row_local, n0 = tn * kTfBN;
+      const uint32_t taddr = tmem + b * kTfBN + (uint32_t(32 * q) << 16);
+      const bool ok = !*s_abort;
+      if (u.t_sk < 0 || (u.kb == 0 && u.ke == sc.iters_per_tile)) {
 #pragma unroll 1
-    for (int c = 0; c < kTfBN; c += 32) {
-      uint32_t r[32];
-      tc_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(c), r);
-      if (row < M && !*s_abort) {
-        float* dst = C + int64_t(row) * ldc + n0 + c;
-        if (n0 + c + 32 <= N) {
+        for (int c = 0; c < kTfBN; c += 32) {
+          uint32_t r[32];
+          tc_ld32(taddr + uint32_t(c), r);
+          if (ok) store_row32(args, row, n0 + c, reinterpret_cast<const float(&)[32]>(r));
+        }
+      } else {
+        // Split tile, as in the FFMA kernel: the sharers publish their partial
+        // sums (float4 j of row r at j * 128 + r, coalesced across a warp) and
+        // the last to arrive adds all of them in CTA order.  The owner of the
+        // tile's first k-slices keeps its partial in TMEM: when every other
+        // sharer has already arrived it is the last and publishes nothing.
+        // All four epilogue warps take the same path through the named
+        // barriers below, also after a timeout (whose output is invalid).
+        const int64_t t_first_iter = int64_t(u.t_sk) * sc.iters_per_tile;
+        const int c_first = sk_owner(sc, t_first_iter);
+        const int c_last = sk_owner(sc, t_first_iter + sc.iters_per_tile - 1);
+        const int others = c_last - c_first;
+        const bool own_first = cta == c_first;
+        bool last = false;
+        if (own_first) {
+          if (etid == 0) *s_last = dev::ld_acquire_gpu(args.counters + u.t_sk) == others ? 1 : 0;
+          dev::named_barrier(1, kTfEpiThreads);
+          last = *s_last != 0;
+          dev::named_barrier(1, kTfEpiThreads);
+        }
+        if (!last) {
+          float4* mine = reinterpret_cast<float4*>(args.partials) + (u.t_sk + cta) * kSlotVec + row_local;
+#pragma unroll 1
+          for (int c = 0; c < kTfBN; c += 32) {
+            uint32_t r[32];
+            tc_ld32(taddr + uint32_t(c), r);
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            reinterpret_cast<float4*>(dst)[v] =
-                make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                            __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-        } else {
+            for (int v = 0; v < 8; ++v)
+              __stcg(mine + (c / 4 + v) * kTfBM,
+                     make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                 __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
+          }
+          __threadfence();
+          dev::named_barrier(1, kTfEpiThreads);
+          if (etid == 0) *s_last = atomicAdd(args.counters + u.t_sk, 1) == others ? 1 : 0;
+          dev::named_barrier(1, kTfEpiThreads);
+          last = *s_last != 0;
+          dev::named_barrier(1, kTfEpiThreads);  // s_last may be rewritten by the next split tile
+        }
+        if (last) {
+          __threadfence();
+          const float4* base = reinterpret_cast<const float4*>(args.partials) + row_local;
+          // 64 columns per step: every slot's 16 loads of a step are in flight together.
+#pragma unroll 1
+          for (int c = 0; c < kTfBN; c += 64) {
+            float sum[64];
+            if (own_first) {
+              uint32_t r[32];
+              tc_ld32(taddr + uint32_t(c), r);
 #pragma unroll
-          for (int v = 0; v < 32; ++v)
-            if (n0 + c + v < N) dst[v] = __uint_as_float(r[v]);
+              for (int i = 0; i < 32; ++i) sum[i] = __uint_as_float(r[i]);
+              tc_ld32(taddr + uint32_t(c + 32), r);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) sum[32 + i] = __uint_as_float(r[i]);
+            } else {
+              const float4* src = base + (u.t_sk + c_first) * kSlotVec + (c / 4) * kTfBM;
+#pragma unroll
+              for (int v = 0; v < 16; ++v) {
+                const float4 x = __ldcg(src + v * kTfBM);
+                sum[4 * v] = x.x;
+                sum[4 * v + 1] = x.y;
+                sum[4 * v + 2] = x.z;
+                sum[4 * v + 3] = x.w;
+              }
+            }
+#pragma unroll 1
+            for (int cc = c_first + 1; cc <= c_last; ++cc) {
+              const float4* src = base + (u.t_sk + cc) * kSlotVec + (c / 4) * kTfBM;
+              float4 x[16];
+#pragma unroll
+              for (int v = 0; v < 16; ++v) x[v] = __ldcg(src + v * kTfBM);
+#pragma unroll
+              for (int v = 0; v < 16; ++v) {
+                sum[4 * v] += x[v].x;
+                sum[4 * v + 1] += x[v].y;
+                sum[4 * v + 2] += x[v].z;
+                sum[4 * v + 3] += x[v].w;
+              }
+            }
+            store_row32(args, row, n0 + c, reinterpret_cast<const float(&)[32]>(sum[0]));
+            store_row32(args, row, n0 + c + 32, reinterpret_cast<const float(&)[32]>(sum[32]));
+          }
+          if (etid == 0) args.counters[u.t_sk] = 0;
         }
       }
+      // The accumulator may be overwritten by the unit after next.
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) dev::mbar_arrive(&acc_empty[b]);
+      ++ui;
     }
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (warp == 1) {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -367,15 +516,12 @@ cudaError_t launch_transpose(const float* B, int64_t ldb, float* Bt, int64_t ldb
 }
 
 cudaError_t launch_tf32_kernel(bool b_mn, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
-                               int M, int N, int K, float* C, int64_t ldc, int group_m,
-                               uint32_t* status, uint64_t limit, cudaStream_t stream) {
-  const int tiles_m = (M + kTfBM - 1) / kTfBM, tiles_n = (N + kTfBN - 1) / kTfBN;
+                               const Tf32Args& args, const Sched& sched, int grid,
+                               cudaStream_t stream) {
   if (b_mn)
-    tf32_kernel<true><<<tiles_m * tiles_n, kTfThreads, kTfSmem, stream>>>(
-        tmap_a, tmap_b, M, N, K, C, ldc, tiles_m, tiles_n, group_m, status, limit);
+    tf32_kernel<true><<<grid, kTfThreads, kTfSmem, stream>>>(tmap_a, tmap_b, args, sched);
   else
-    tf32_kernel<false><<<tiles_m * tiles_n, kTfThreads, kTfSmem, stream>>>(
-        tmap_a, tmap_b, M, N, K, C, ldc, tiles_m, tiles_n, group_m, status, limit);
+    tf32_kernel<false><<<grid, kTfThreads, kTfSmem, stream>>>(tmap_a, tmap_b, args, sched);
   return cudaGetLastError();
 }
 

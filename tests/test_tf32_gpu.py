@@ -151,3 +151,19 @@ def test_tf32_integers_exact_through_both_b_paths():
         C = sg.sgemm_tf32(A.cuda(), Bd)
         torch.cuda.synchronize()
         check_exact(C.cpu().numpy(), ref, "tf32 integers")
+
+
+@pytest.mark.parametrize("shape", [(1000, 1000, 2048), (4096, 4096, 512)], ids=lambda s: "x".join(map(str, s)))
+def test_tf32_stream_k_deterministic_and_within_bound(shape):
+    """Split tiles (Stream-K) are summed in a fixed order: repeated calls agree bit for bit."""
+    M, N, K = shape
+    A = workloads.matrix(M, K, "uniform", 97, 0)
+    B = workloads.matrix(K, N, "uniform", 97, 1)
+    dA, dB = A.cuda(), B.cuda()
+    C1 = sg.sgemm_tf32(dA, dB)
+    C2 = sg.sgemm_tf32(dA, dB)
+    torch.cuda.synchronize()
+    assert torch.equal(C1, C2)
+    r, c = workloads.sample_indices(M, N, 2048, 97)
+    ref, E = oracle.sgemm_entries_f64(A, B, r.numpy(), c.numpy())
+    check_tf32(C1[r.cuda(), c.cuda()].cpu().numpy(), ref, E, K, f"tf32 {shape}")
