@@ -178,12 +178,18 @@ def ffma_peak_tflops(sms: int, mhz: float) -> float:
     return sms * FFMA_PER_CLK_PER_SM * 2 * mhz * 1e6 / 1e12
 
 
+# The files the tile kernel is compiled from, in a fixed order.
+KERNEL_SOURCES = ("sgemm_tile.cu", "sgemm_sched.cuh", "sgemm_device.cuh", "sgemm_internal.h")
+
+
 def kernel_source_digest() -> str:
-    """SHA-256 of the tile kernel's source: profile counters apply only to this exact kernel."""
+    """SHA-256 over the tile kernel's sources: profile counters apply only to this exact kernel."""
     import hashlib
-    path = os.path.join(ROOT, "dense_fp32_gemm_03_gb300", "csrc", "sgemm_tile.cu")
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "dense_fp32_gemm_03_gb300", "csrc", name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
 
 
 def measured_traffic(workload: str):
