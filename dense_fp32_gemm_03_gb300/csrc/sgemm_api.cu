@@ -50,6 +50,7 @@ struct DeviceState {
   int sms = 0;
   int ctas_per_sm[gb300::kTileConfigs] = {};
   int tf32_ctas_per_sm = 0;
+  int tf32_pairs = 0;  // CTA pairs of the 2-SM TF32 kernel that run at once (0: not used)
   uint32_t* status = nullptr;
 };
 
@@ -100,6 +101,8 @@ sgemm_status_t device_state(DeviceState** out, int* dev_out) {
       }
       if (gb300::specialized_prepare() < 0) st.init_status = SGEMM_ERR_LAUNCH;
       st.tf32_ctas_per_sm = gb300::tf32_prepare();
+      st.tf32_pairs = gb300::tf32_pair_prepare();
+      if (st.tf32_pairs < 0) st.tf32_pairs = 0;
       if (st.tf32_ctas_per_sm <= 0) st.init_status = SGEMM_ERR_LAUNCH;
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) {
@@ -558,14 +561,18 @@ sgemm_status_t sgemm_tf32(int64_t M, int64_t N, int64_t K, const float* A, int64
   // K.  At most one wave: one tile per CTA, since reducing 128 KB partial
   // tiles then costs more than the idle SMs (measured on GB300 from 1024^3
   // to 2048^3; from 2560^3 up the split schedule wins).
-  const int64_t resident = int64_t(ds->sms) * ds->tf32_ctas_per_sm;
-  const int bm = gb300::tf32_tile_m(), bn = gb300::tf32_tile_n(), bk = gb300::tf32_tile_k();
+  const bool pair = ds->tf32_pairs > 0;
+  const int64_t resident = pair ? int64_t(ds->tf32_pairs) : int64_t(ds->sms) * ds->tf32_ctas_per_sm;
+  const int bm = pair ? gb300::tf32_pair_tile_m() : gb300::tf32_tile_m();
+  const int bn = pair ? gb300::tf32_pair_tile_n() : gb300::tf32_tile_n();
+  const int bk = gb300::tf32_tile_k();
   const int64_t tiles = ((M + bm - 1) / bm) * ((N + bn - 1) / bn);
   const gb300::LaunchPlan lp = gb300::plan_launch(M, N, K, bm, bn, bk, resident, tiles > resident);
-  if (!lp.ok || lp.grid > kInt32Max || lp.sc.sk_tiles > kMaxSplitTiles)
+  if (!lp.ok || lp.grid > kInt32Max ||
+      lp.sc.sk_tiles * (pair ? 2 : 1) > kMaxSplitTiles)
     return SGEMM_ERR_UNSUPPORTED;
   // Workspace: [counters][partial slots][B^T when B cannot be read in place].
-  const size_t slot_bytes = size_t(gb300::tf32_tile_m()) * gb300::tf32_tile_n() * 4;
+  const size_t slot_bytes = size_t(bm) * bn * 4;
   const size_t partial_bytes = size_t(lp.slots) * slot_bytes;
   // B is read in place as an MN-major operand when TMA can address it;
   // otherwise B^T (N x K, rows padded to a multiple of 4 floats) is written
@@ -608,8 +615,8 @@ sgemm_status_t sgemm_tf32(int64_t M, int64_t N, int64_t K, const float* A, int64
                                 b_mn ? cuuint64_t(K) : cuuint64_t(N)};
     const cuuint64_t strides[1] = {cuuint64_t(ldb) * 4};
     const cuuint32_t box[2] = {
-        b_mn ? cuuint32_t(gb300::tf32_b_chunk()) : cuuint32_t(gb300::tf32_tile_k()),
-        b_mn ? cuuint32_t(gb300::tf32_tile_k()) : cuuint32_t(gb300::tf32_tile_n())};
+        b_mn ? cuuint32_t(gb300::tf32_b_chunk()) : cuuint32_t(bk),
+        b_mn ? cuuint32_t(bk) : cuuint32_t(pair ? bn / 2 : bn)};
     if (g_encode(&tmap_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(b_src), dims,
                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                  b_mn ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B,
@@ -625,10 +632,10 @@ sgemm_status_t sgemm_tf32(int64_t M, int64_t N, int64_t K, const float* A, int64
   args.partials = ws ? reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes) : nullptr;
   args.status = ds->status;
   args.wait_limit_ns = kDefaultWaitLimitNs;
-  return gb300::launch_tf32_kernel(b_mn, tmap_a, tmap_b, args, lp.sc, int(lp.grid), stream) ==
-                 cudaSuccess
-             ? SGEMM_OK
-             : SGEMM_ERR_LAUNCH;
+  const cudaError_t e =
+      pair ? gb300::launch_tf32_pair_kernel(b_mn, tmap_a, tmap_b, args, lp.sc, int(lp.grid), stream)
+           : gb300::launch_tf32_kernel(b_mn, tmap_a, tmap_b, args, lp.sc, int(lp.grid), stream);
+  return e == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
 }
 
 sgemm_status_t sgemm_query_device_status(cudaStream_t stream, uint32_t* detail) {

@@ -184,6 +184,18 @@ cudaError_t launch_tf32_kernel(bool b_mn, const CUtensorMap& tmap_a, const CUten
                                const Tf32Args& args, const Sched& sched, int grid,
                                cudaStream_t stream);
 
+// CTA-pair TF32 kernel (tcgen05.mma.cta_group::2): 256 x 256 tiles per pair of SMs.  Returns
+// the CTA pairs that can run at once, or <= 0 if none.
+int tf32_pair_prepare();
+int tf32_pair_tile_m();
+int tf32_pair_tile_n();
+// tmap_b as for launch_tf32_kernel, except that a transposed Bt is read in boxes {32, 128};
+// `sched` is plan_launch over 256 x 256 x 32 tiles for `pairs` persistent pairs.  Split
+// tiles use two counters and two partial slots (one per CTA of the pair) each.
+cudaError_t launch_tf32_pair_kernel(bool b_mn, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                                    const Tf32Args& args, const Sched& sched, int pairs,
+                                    cudaStream_t stream);
+
 cudaError_t launch_guarded_kernel(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
                                   const float* B, int64_t ldb, float* C, int64_t ldc, int scaled,
                                   float alpha, float beta, cudaStream_t stream);

@@ -407,6 +407,355 @@ __global__ void __launch_bounds__(kTfThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// CTA-pair kernel: tcgen05.mma.cta_group::2 over 256 x 256 tiles.
+//
+// A cluster of two CTAs on two SMs computes one 256 x 256 tile.  Each CTA
+// stages its own 128 rows of A and its own 128 columns of B per 32-deep
+// k-slice (32 KB, so six stages fit); the even CTA (the leader) issues the
+// M = 256, N = 256 MMAs, which read both CTAs' shared memory at the same
+// offsets and leave rows [128 r, 128 r + 128) of the tile in the TMEM of CTA
+// r.  Both CTAs' copies complete on the leader's full barrier; the leader's
+// commits are multicast to the barriers of both CTAs; each CTA's epilogue
+// reads its own TMEM and tells the leader, across the cluster, when the
+// accumulator may be reused.  The work decomposition runs over CTA pairs.
+constexpr int kPrBM = 256, kPrBN = 256, kPrBK = 32, kPrStages = 6;
+constexpr int kPrRows = kPrBM / 2, kPrCols = kPrBN / 2;      // per CTA
+constexpr uint32_t kPrAStageBytes = kPrRows * kPrBK * 4;    // 16 KB
+constexpr uint32_t kPrBStageBytes = kPrCols * kPrBK * 4;    // 16 KB
+// Two 256-column accumulators per CTA.  Both CTAs execute the cta_group::2
+// allocation and receive the same address (measured on GB300).
+constexpr uint32_t kPrTmemCols = 512;
+constexpr int kPrAccBufs = int(kPrTmemCols / kPrBN);          // accumulators per CTA
+constexpr int kPrBarriers = 2 * kPrStages + 2 * 2 + 1;
+constexpr size_t kPrSmem = 1024 + kPrStages * size_t(kPrAStageBytes + kPrBStageBytes) +
+                           kPrBarriers * 8 + 16;
+
+__host__ __device__ constexpr uint32_t pr_idesc(uint32_t b_mn) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | (0u << 15) | (b_mn << 16) |
+         (uint32_t(kPrBN >> 3) << 17) | (uint32_t(kPrBM >> 4) << 24);
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address of this CTA's shared-memory location `p` in the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(dev::smem_addr(p)), "r"(rank));
+  return d;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+__device__ __forceinline__ void pr_tma_load(void* dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                            uint32_t bar_cluster_addr) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dev::smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster_addr)
+      : "memory");
+}
+
+template <uint32_t kIdesc>
+__device__ __forceinline__ void pr_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "n"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives on the barrier at `bar`'s offset in both CTAs of the pair once every
+// tcgen05 operation this thread issued so far completed.
+__device__ __forceinline__ void pr_commit_both(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(dev::smem_addr(bar)),
+      "h"(uint16_t(3))
+      : "memory");
+}
+
+__device__ __forceinline__ void pr_commit_own(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   dev::smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void remote_arrive(uint32_t bar_cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr)
+               : "memory");
+}
+
+template <bool B_MN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTfThreads, 1)
+    tf32_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                     const Tf32Args args, const Sched sc) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = dev::smem_addr(smem_raw);
+  unsigned char* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  unsigned char* sA = smem;
+  unsigned char* sB = smem + kPrStages * kPrAStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kPrStages * kPrBStageBytes);  // used in the leader
+  uint64_t* empty = full + kPrStages;
+  uint64_t* acc_full = empty + kPrStages;  // [2]
+  uint64_t* acc_empty = acc_full + 2;      // [2], used in the leader: 4 warps x 2 CTAs arrive
+  uint64_t* drain = acc_empty + 2;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(drain + 1);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(drain + 1) + 1;
+  int* s_last = reinterpret_cast<int*>(drain + 1) + 2;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1, pairs = gridDim.x >> 1;
+  const uint64_t limit = args.wait_limit_ns;
+
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     dev::smem_addr(const_cast<uint32_t*>(tmem_slot))),
+                 "r"(kPrTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPrStages; ++s) {
+      dev::mbar_init(&full[s], 1);
+      dev::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      dev::mbar_init(&acc_full[b], 1);
+      dev::mbar_init(&acc_empty[b], 2 * kTfEpiWarps);
+    }
+    dev::mbar_init(drain, 1);
+    *s_abort = 0;
+    dev::mbar_init_fence();
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  cluster_sync_all();  // the peer's barriers exist before anything signals them
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_slot;
+
+  auto fail = [&]() {
+    if (!*s_abort) {
+      *s_abort = 1;
+      dev::record_status(args.status, kStatusTimeout, kWaitTileStage);
+    }
+  };
+
+  if (warp == 0) {
+    // ---- TMA producer (both CTAs): this CTA's rows of A and columns of B,
+    // completing on the leader's full barrier.
+    if (dev::elect_one()) {
+      dev::tma_prefetch_desc(&tmap_a);
+      dev::tma_prefetch_desc(&tmap_b);
+    }
+    KCursor c;
+    c.init(sc, pair, pairs);
+    uint32_t i = 0;
+    for (; c.valid; ++i, c.advance(sc, pairs)) {
+      const uint32_t s = i % kPrStages, n = i / kPrStages;
+      if (n > 0 && !dev::mbar_wait_abortable(&empty[s], (n - 1) & 1u, limit, s_abort)) fail();
+      if (*s_abort) break;
+      const int k0 = (c.u.kb + c.j) * kPrBK;
+      const int m0 = c.tm * kPrBM + int(rank) * kPrRows, n0 = c.tn * kPrBN + int(rank) * kPrCols;
+      if (dev::elect_one()) {
+        const uint32_t bar = peer_addr(&full[s], 0);
+        if (leader) dev::mbar_arrive_expect_tx(&full[s], 2 * (kPrAStageBytes + kPrBStageBytes));
+        pr_tma_load(sA + s * kPrAStageBytes, &tmap_a, k0, m0, bar);
+        if constexpr (B_MN) {
+#pragma unroll
+          for (int j = 0; j < kPrCols / kTfBChunk; ++j)
+            pr_tma_load(sB + s * kPrBStageBytes + j * kTfBChunkBytes, &tmap_b, n0 + j * kTfBChunk, k0,
+                        bar);
+        } else {
+          pr_tma_load(sB + s * kPrBStageBytes, &tmap_b, k0, n0, bar);
+        }
+      }
+      __syncwarp();
+    }
+    // After a failure, this CTA's last copies complete on the leader's barrier,
+    // which it cannot observe: give them a bounded grace period (a copy lands
+    // within microseconds) before shared memory is released.
+    if (*s_abort) {
+      const uint64_t t0 = dev::global_timer_ns();
+      while (dev::global_timer_ns() - t0 < 100000ull) __nanosleep(1000);
+    }
+  } else if (warp == 1) {
+    if (leader) {
+      // ---- MMA issuer (leader only)
+      WorkIter w;
+      w.init(sc, pair);
+      Unit u;
+      uint32_t it = 0, ui = 0;
+      while (w.next(sc, pairs, u)) {
+        const uint32_t b = ui % kPrAccBufs, nb = ui / kPrAccBufs;
+        if (nb > 0 && !dev::mbar_wait_abortable(&acc_empty[b], (nb - 1) & 1u, limit, s_abort))
+          fail();
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t d = tmem + b * kPrBN;
+        const int nk = u.ke - u.kb;
+        for (int j = 0; j < nk; ++j, ++it) {
+          const uint32_t s = it % kPrStages;
+          if (!dev::mbar_wait_abortable(&full[s], (it / kPrStages) & 1u, limit, s_abort)) fail();
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          if (dev::elect_one()) {
+            if (!*s_abort) {
+              const uint64_t a_desc = sw128_kmajor_desc(dev::smem_addr(sA + s * kPrAStageBytes));
+              const uint32_t b_addr = dev::smem_addr(sB + s * kPrBStageBytes);
+              const uint64_t b_desc =
+                  B_MN ? sw128a32_mnmajor_desc(b_addr) : sw128_kmajor_desc(b_addr);
+              constexpr uint64_t kBStep = B_MN ? 1024 / 16 : 32 / 16;
+#pragma unroll
+              for (int k = 0; k < kPrBK / 8; ++k)
+                pr_mma<pr_idesc(B_MN ? 1u : 0u)>(d, a_desc + 2 * k, b_desc + kBStep * k,
+                                                 (j | k) != 0 ? 1u : 0u);
+            }
+            pr_commit_both(&empty[s]);
+          }
+          __syncwarp();
+        }
+        if (dev::elect_one()) pr_commit_both(&acc_full[b]);
+        __syncwarp();
+        ++ui;
+      }
+      if (dev::elect_one()) pr_commit_own(drain);
+      __syncwarp();
+      dev::mbar_wait(drain, 0u, limit);
+    }
+  } else {
+    // ---- epilogue (both CTAs): rows [128 rank, 128 rank + 128) of each tile
+    const int q = warp & 3;
+    const int row_local = 32 * q + lane;
+    const int etid = threadIdx.x - 64;
+    constexpr int64_t kHalfVec = int64_t(kPrRows) * kPrBN / 4;  // one CTA's partial, in float4
+    WorkIter w;
+    w.init(sc, pair);
+    Unit u;
+    uint32_t ui = 0;
+    while (w.next(sc, pairs, u)) {
+      const uint32_t b = ui % kPrAccBufs, nb = ui / kPrAccBufs;
+      if (!dev::mbar_wait_abortable(&acc_full[b], nb & 1u, limit, s_abort)) fail();
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      int tm, tn;
+      tile_coords(sc, u.tile, tm, tn);
+      const int row = tm * kPrBM + int(rank) * kPrRows + row_local, n0 = tn * kPrBN;
+      const uint32_t taddr = tmem + b * kPrBN + (uint32_t(32 * q) << 16);
+      const bool ok = !*s_abort;
+      if (u.t_sk < 0 || (u.kb == 0 && u.ke == sc.iters_per_tile)) {
+#pragma unroll 1
+        for (int c = 0; c < kPrBN; c += 32) {
+          uint32_t r[32];
+          tc_ld32(taddr + uint32_t(c), r);
+          if (ok) store_row32(args, row, n0 + c, reinterpret_cast<const float(&)[32]>(r));
+        }
+      } else {
+        // Split tile, per CTA half: counters[2 t + rank], slot 2 (t + pair) + rank.
+        const int64_t t_first_iter = int64_t(u.t_sk) * sc.iters_per_tile;
+        const int c_first = sk_owner(sc, t_first_iter);
+        const int c_last = sk_owner(sc, t_first_iter + sc.iters_per_tile - 1);
+        const int others = c_last - c_first;
+        const bool own_first = pair == c_first;
+        int32_t* counter = args.counters + 2 * u.t_sk + int(rank);
+        bool last = false;
+        if (own_first) {
+          if (etid == 0) *s_last = dev::ld_acquire_gpu(counter) == others ? 1 : 0;
+          dev::named_barrier(1, kTfEpiThreads);
+          last = *s_last != 0;
+          dev::named_barrier(1, kTfEpiThreads);
+        }
+        if (!last) {
+          float4* mine = reinterpret_cast<float4*>(args.partials) +
+                         (2 * (u.t_sk + pair) + int(rank)) * kHalfVec + row_local;
+#pragma unroll 1
+          for (int c = 0; c < kPrBN; c += 32) {
+            uint32_t r[32];
+            tc_ld32(taddr + uint32_t(c), r);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              __stcg(mine + (c / 4 + v) * kPrRows,
+                     make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                 __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
+          }
+          __threadfence();
+          dev::named_barrier(1, kTfEpiThreads);
+          if (etid == 0) *s_last = atomicAdd(counter, 1) == others ? 1 : 0;
+          dev::named_barrier(1, kTfEpiThreads);
+          last = *s_last != 0;
+          dev::named_barrier(1, kTfEpiThreads);
+        }
+        if (last) {
+          __threadfence();
+          const float4* base = reinterpret_cast<const float4*>(args.partials) + row_local;
+#pragma unroll 1
+          for (int c = 0; c < kPrBN; c += 64) {
+            float sum[64];
+            if (own_first) {
+              uint32_t r[32];
+              tc_ld32(taddr + uint32_t(c), r);
+#pragma unroll
+              for (int k = 0; k < 32; ++k) sum[k] = __uint_as_float(r[k]);
+              tc_ld32(taddr + uint32_t(c + 32), r);
+#pragma unroll
+              for (int k = 0; k < 32; ++k) sum[32 + k] = __uint_as_float(r[k]);
+            } else {
+              const float4* src =
+                  base + (2 * (u.t_sk + c_first) + int(rank)) * kHalfVec + (c / 4) * kPrRows;
+#pragma unroll
+              for (int v = 0; v < 16; ++v) {
+                const float4 x = __ldcg(src + v * kPrRows);
+                sum[4 * v] = x.x;
+                sum[4 * v + 1] = x.y;
+                sum[4 * v + 2] = x.z;
+                sum[4 * v + 3] = x.w;
+              }
+            }
+#pragma unroll 1
+            for (int cc = c_first + 1; cc <= c_last; ++cc) {
+              const float4* src = base + (2 * (u.t_sk + cc) + int(rank)) * kHalfVec + (c / 4) * kPrRows;
+              float4 x[16];
+#pragma unroll
+              for (int v = 0; v < 16; ++v) x[v] = __ldcg(src + v * kPrRows);
+#pragma unroll
+              for (int v = 0; v < 16; ++v) {
+                sum[4 * v] += x[v].x;
+                sum[4 * v + 1] += x[v].y;
+                sum[4 * v + 2] += x[v].z;
+                sum[4 * v + 3] += x[v].w;
+              }
+            }
+            store_row32(args, row, n0 + c, reinterpret_cast<const float(&)[32]>(sum[0]));
+            store_row32(args, row, n0 + c + 32, reinterpret_cast<const float(&)[32]>(sum[32]));
+          }
+          if (etid == 0) *counter = 0;
+        }
+      }
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) remote_arrive(peer_addr(&acc_empty[b], 0));
+      ++ui;
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  cluster_sync_all();  // nothing of either CTA is still signalled or read by the other
+  if (warp == 1) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kPrTmemCols)
+                 : "memory");
+  }
+}
+
 // Bt[n][k] = B[k][n] through 32 x 33 shared tiles (coalesced on both sides).
 __global__ void __launch_bounds__(256)
     transpose_kernel(const float* __restrict__ B, int64_t ldb, float* __restrict__ Bt,
@@ -512,6 +861,35 @@ cudaError_t launch_transpose(const float* B, int64_t ldb, float* Bt, int64_t ldb
     const dim3 grid(unsigned((int64_t(N) + 31) / 32), unsigned(k_tiles < 65535 ? k_tiles : 65535));
     transpose_kernel<<<grid, dim3(32, 8), 0, stream>>>(B, ldb, Bt, ldbt, K, N);
   }
+  return cudaGetLastError();
+}
+
+int tf32_pair_prepare() {
+  if (cudaFuncSetAttribute(tf32_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(kPrSmem)) != cudaSuccess ||
+      cudaFuncSetAttribute(tf32_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(kPrSmem)) != cudaSuccess)
+    return -1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kTfThreads, 1, 1);
+  cfg.dynamicSmemBytes = kPrSmem;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, tf32_pair_kernel<true>, &cfg) != cudaSuccess)
+    return -1;
+  return clusters;
+}
+
+int tf32_pair_tile_m() { return kPrBM; }
+int tf32_pair_tile_n() { return kPrBN; }
+
+cudaError_t launch_tf32_pair_kernel(bool b_mn, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                                    const Tf32Args& args, const Sched& sched, int pairs,
+                                    cudaStream_t stream) {
+  if (b_mn)
+    tf32_pair_kernel<true><<<2 * pairs, kTfThreads, kPrSmem, stream>>>(tmap_a, tmap_b, args, sched);
+  else
+    tf32_pair_kernel<false><<<2 * pairs, kTfThreads, kPrSmem, stream>>>(tmap_a, tmap_b, args, sched);
   return cudaGetLastError();
 }
 
