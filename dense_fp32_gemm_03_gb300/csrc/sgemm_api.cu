@@ -103,6 +103,9 @@ sgemm_status_t device_state(DeviceState** out, int* dev_out) {
       st.tf32_ctas_per_sm = gb300::tf32_prepare();
       st.tf32_pairs = gb300::tf32_pair_prepare();
       if (st.tf32_pairs < 0) st.tf32_pairs = 0;
+      // SGEMM_TF32_PAIRS=0 selects the single-SM TF32 kernel (for testing that path).
+      const char* pairs_env = std::getenv("SGEMM_TF32_PAIRS");
+      if (pairs_env != nullptr && std::strcmp(pairs_env, "0") == 0) st.tf32_pairs = 0;
       if (st.tf32_ctas_per_sm <= 0) st.init_status = SGEMM_ERR_LAUNCH;
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) {

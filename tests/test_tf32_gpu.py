@@ -167,3 +167,39 @@ def test_tf32_stream_k_deterministic_and_within_bound(shape):
     r, c = workloads.sample_indices(M, N, 2048, 97)
     ref, E = oracle.sgemm_entries_f64(A, B, r.numpy(), c.numpy())
     check_tf32(C1[r.cuda(), c.cuda()].cpu().numpy(), ref, E, K, f"tf32 {shape}")
+
+
+_SINGLE_SM_SCRIPT = r"""
+import sys, numpy as np, torch
+sys.path.insert(0, {root!r})
+sys.path.insert(0, {tests!r})
+import oracle
+import dense_fp32_gemm_03_gb300 as sg
+from dense_fp32_gemm_03_gb300 import workloads
+for (M, N, K) in [(256, 512, 384), (1000, 1000, 2048), (4096, 4096, 512)]:
+    A = workloads.matrix(M, K, "int8range", 98, 0)
+    B = workloads.matrix(K, N, "int8range", 98, 1)
+    C = sg.sgemm_tf32(A.cuda(), B.cuda())
+    torch.cuda.synchronize()
+    r, c = workloads.sample_indices(M, N, 2048, 98)
+    ref, E = oracle.sgemm_entries_f64(A, B, r.numpy(), c.numpy())
+    assert E.max() < 2 ** 24
+    got = C[r.cuda(), c.cuda()].cpu().numpy().astype(np.float64)
+    assert np.array_equal(got, ref), (M, N, K)
+assert sg.query_device_status() == (0, 0)
+print("single-SM path ok")
+"""
+
+
+def test_tf32_single_sm_kernel_in_a_subprocess():
+    """The single-SM kernel (used where no CTA pair fits) stays exact on integers."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    script = _SINGLE_SM_SCRIPT.format(root=root, tests=os.path.join(root, "tests"))
+    env = dict(os.environ, SGEMM_TF32_PAIRS="0")
+    r = subprocess.run([sys.executable, "-c", script], env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "single-SM path ok" in r.stdout
