@@ -4,7 +4,7 @@ The product is the C-ABI library ``libsgemm.so`` (``include/sgemm.h``); this
 package builds it (``_build``), binds it (``binding``) and provides the seeded
 synthetic workloads (``workloads``).
 """
-from .binding import (AUTO, GUARDED, SPECIALIZED, STAGED, STREAMK, STREAMK_SMALL, TILED, TILED_SMALL, VARIANTS,
+from .binding import (AUTO, GUARDED, SMALL, SPECIALIZED, STAGED, STREAMK, STREAMK_SMALL, TILED, TILED_SMALL, VARIANTS,
                       SgemmError, debug_expire_wait, load, query_device_status,
                       release_workspaces, select_variant, sgemm, sgemm_ex, sgemm_raw, sgemm_tf32, status_string,
                       ROW_MAJOR, COL_MAJOR,
@@ -13,4 +13,4 @@ from .binding import (AUTO, GUARDED, SPECIALIZED, STAGED, STREAMK, STREAMK_SMALL
 __all__ = ["sgemm", "sgemm_ex", "ROW_MAJOR", "COL_MAJOR", "sgemm_tf32", "sgemm_raw", "select_variant", "workspace_size", "query_device_status",
            "debug_expire_wait", "release_workspaces", "status_string", "variant_name", "load",
            "SgemmError", "VARIANTS", "AUTO", "GUARDED", "TILED", "STREAMK", "TILED_SMALL",
-           "STREAMK_SMALL", "STAGED", "SPECIALIZED"]
+           "STREAMK_SMALL", "STAGED", "SPECIALIZED", "SMALL"]

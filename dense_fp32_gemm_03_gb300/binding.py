@@ -15,11 +15,11 @@ from . import _build
 # sgemm_status_t
 OK, ERR_INVALID_VALUE, ERR_LAUNCH, ERR_TIMEOUT, ERR_UNSUPPORTED, ERR_ALLOC = range(6)
 # sgemm_variant_t
-AUTO, GUARDED, TILED, STREAMK, TILED_SMALL, STREAMK_SMALL, STAGED, SPECIALIZED = (
-    -1, 0, 1, 2, 3, 4, 5, 6)
+AUTO, GUARDED, TILED, STREAMK, TILED_SMALL, STREAMK_SMALL, STAGED, SPECIALIZED, SMALL = (
+    -1, 0, 1, 2, 3, 4, 5, 6, 7)
 VARIANTS = {"guarded": GUARDED, "tiled": TILED, "streamk": STREAMK,
             "tiled_small": TILED_SMALL, "streamk_small": STREAMK_SMALL, "staged": STAGED,
-            "specialized": SPECIALIZED}
+            "specialized": SPECIALIZED, "small": SMALL}
 
 # Every entry point include/sgemm.h declares.
 EXPORTS = ("sgemm", "sgemm_variant", "sgemm_select_variant", "sgemm_workspace_size",

@@ -39,6 +39,17 @@ constexpr double kGuardedTflops = 23.0;     // large products
 constexpr double kGuardedStepUs = 1.6;      // one 16-deep step of a CTA (a global-load round trip)
 constexpr double kGuardedCtasPerSm = 4.0;   // 256 threads x 64 registers
 constexpr double kCopyBytesPerUs = 4.5e6;
+// Small-product kernel: CTAs per SM it is sized for (128 threads x 128
+// registers); the time of one 16-deep slice of a 64 x 64 tile when the SM
+// runs one CTA (latency bound) and when it runs four (arithmetic bound);
+// the fixed cost of a launch; the reduction cost per share of a split tile
+// (the last share reads every other share's 16 KB partial).  Fitted to
+// GB300 timings with forced split counts from 256^3 to 768^3.
+constexpr int kSmallCtasPerSm = 4;
+constexpr double kSmallSliceUs = 0.75;
+constexpr double kSmallFullSliceUs = 2.3;
+constexpr double kSmallFixedUs = 5.0;
+constexpr double kSmallShareUs = 0.45;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -175,6 +186,9 @@ struct Plan {
   Sched sc{};
   int grid = 0;
   size_t partial_bytes = 0;
+  // The small-product kernel's decomposition: 64 x 64 tiles, K in `splits` shares.
+  int64_t small_tiles = 0, small_tiles_n = 0;
+  int splits = 1, k_chunk = 0;
   size_t workspace_bytes() const { return partial_bytes ? kCounterBytes + partial_bytes : 0; }
 };
 
@@ -213,13 +227,59 @@ Staging make_staging(const Plan& p, int64_t M, int64_t N, int64_t K, bool stage_
 
 bool is_fast(int v) {
   return v == SGEMM_VARIANT_TILED || v == SGEMM_VARIANT_STREAMK ||
-         v == SGEMM_VARIANT_TILED_SMALL || v == SGEMM_VARIANT_STREAMK_SMALL;
+         v == SGEMM_VARIANT_TILED_SMALL || v == SGEMM_VARIANT_STREAMK_SMALL ||
+         v == SGEMM_VARIANT_SMALL;
+}
+
+// Estimated duration (microseconds) of the small-product kernel for `grid`
+// CTAs of `slices` 16-deep slices each, the tiles split into `splits` shares.
+double small_cost_us(int64_t grid, int64_t slices, int64_t splits, const DeviceState& ds) {
+  const double per_sm = std::ceil(double(grid) / double(ds.sms));
+  const double waves = std::ceil(per_sm / kSmallCtasPerSm);
+  const double busy = per_sm < kSmallCtasPerSm ? per_sm : double(kSmallCtasPerSm);
+  double slice_us = kSmallFullSliceUs * busy / kSmallCtasPerSm;
+  if (slice_us < kSmallSliceUs) slice_us = kSmallSliceUs;
+  const double reduce = splits > 1 ? 0.5 + kSmallShareUs * double(splits) : 0.0;
+  return kSmallFixedUs + waves * double(slices) * slice_us + reduce;
+}
+
+// The small-product kernel: the number of K shares per tile (a power of two,
+// at least two 16-deep slices per share) with the lowest estimated time.
+bool make_small_plan(int64_t M, int64_t N, int64_t K, const DeviceState& ds, Plan* p) {
+  const gb300::SmallShape ss = gb300::small_shape();
+  const int64_t tiles_n = (N + ss.bn - 1) / ss.bn;
+  const int64_t tiles = ((M + ss.bm - 1) / ss.bm) * tiles_n;
+  const int64_t kslices = (K + ss.bk - 1) / ss.bk;
+  if (tiles > kInt32Max || tiles_n > kInt32Max || kslices * ss.bk > kInt32Max) return false;
+  double best = 1e300;
+  int64_t best_splits = 1, best_chunk = kslices * ss.bk;
+  for (int64_t want = 1; want == 1 || (want <= kslices / 2 && tiles * want <= kInt32Max);
+       want *= 2) {
+    const int64_t chunk_slices = (kslices + want - 1) / want;
+    const int64_t splits = (kslices + chunk_slices - 1) / chunk_slices;
+    if (splits > 1 && tiles > kMaxSplitTiles) break;
+    const double cost = small_cost_us(tiles * splits, chunk_slices, splits, ds);
+    if (cost < best * 0.999) {
+      best = cost;
+      best_splits = splits;
+      best_chunk = chunk_slices * ss.bk;
+    }
+  }
+  if (tiles * best_splits > kInt32Max) return false;
+  p->small_tiles = tiles;
+  p->small_tiles_n = tiles_n;
+  p->splits = int(best_splits);
+  p->k_chunk = int(best_chunk);
+  p->grid = int(tiles * best_splits);
+  p->partial_bytes = best_splits > 1 ? size_t(tiles * best_splits) * ss.bm * ss.bn * 4 : 0;
+  return true;
 }
 
 // Work decomposition of a fast variant.
 bool make_plan(int variant, int64_t M, int64_t N, int64_t K, const DeviceState& ds, Plan* p) {
   p->variant = variant;
   if (!is_fast(variant)) return true;
+  if (variant == SGEMM_VARIANT_SMALL) return make_small_plan(M, N, K, ds, p);
   p->cfg = (variant == SGEMM_VARIANT_TILED_SMALL || variant == SGEMM_VARIANT_STREAMK_SMALL)
                ? g_cfg_small
                : g_cfg_large;
@@ -254,9 +314,12 @@ int find_specialized(const Plan& p, int64_t M, int64_t N, int64_t K, const Devic
 // The model was fitted to measured GB300 timings of the compiled
 // configurations: every CTA slot streams its k-tiles at a fixed efficiency
 // of the FFMA peak (86% with 8x16 patches, 80% with 8x8), plus a fixed cost
-// per launch and, when tiles are split, the time the last CTA of a tile
-// spends reading the partial sums back.
+// per launch (6 us: start-up and tail, fitted from 256^3 to 1280^3) and,
+// when tiles are split, the time the last CTA of a tile spends reading the
+// partial sums back.
 double plan_cost_us(const Plan& p, const DeviceState& ds) {
+  if (p.variant == SGEMM_VARIANT_SMALL)
+    return small_cost_us(p.grid, p.k_chunk / 16, p.splits, ds);
   const TileShape ts = gb300::tile_shape(p.cfg);
   const int cps = ds.ctas_per_sm[p.cfg] > 0 ? ds.ctas_per_sm[p.cfg] : 1;
   const double flop_per_us_per_sm = 128.0 * 2.0 * 2070.0;  // FFMA lanes x 2 x max clock (MHz)
@@ -268,7 +331,7 @@ double plan_cost_us(const Plan& p, const DeviceState& ds) {
       p.grid == p.sc.dp_tiles) {
     // One tile per CTA: whole waves of CTA slots.
     const int64_t waves = (int64_t(p.sc.dp_tiles) + resident - 1) / resident;
-    return 8.0 + double(waves) * ipt * ktile_us;
+    return 6.0 + double(waves) * ipt * ktile_us;
   }
   const double dp_waves = double(p.sc.dp_tiles) / double(resident);
   double iters = dp_waves * ipt;
@@ -280,7 +343,7 @@ double plan_cost_us(const Plan& p, const DeviceState& ds) {
     const double segments = std::ceil(double(p.sc.sk_ctas) / double(p.sc.sk_tiles)) + 1.0;
     fixup = 0.015 * tile_kb * segments;
   }
-  return 10.0 + iters * ktile_us + fixup;
+  return 6.0 + iters * ktile_us + fixup;
 }
 
 // Estimated duration (microseconds) of the bounds-checked kernel, fitted to
@@ -309,8 +372,8 @@ double staging_cost_us(int64_t M, int64_t N, int64_t K, bool stage_a, bool stage
 int select_fast(int64_t M, int64_t N, int64_t K, const DeviceState& ds, double* cost_out) {
   int best = SGEMM_VARIANT_STREAMK;
   double best_cost = 1e300;
-  const int candidates[4] = {SGEMM_VARIANT_STREAMK, SGEMM_VARIANT_STREAMK_SMALL,
-                             SGEMM_VARIANT_TILED, SGEMM_VARIANT_TILED_SMALL};
+  const int candidates[5] = {SGEMM_VARIANT_STREAMK, SGEMM_VARIANT_STREAMK_SMALL,
+                             SGEMM_VARIANT_TILED, SGEMM_VARIANT_TILED_SMALL, SGEMM_VARIANT_SMALL};
   for (int v : candidates) {
     Plan p;
     if (!make_plan(v, M, N, K, ds, &p)) continue;
@@ -468,6 +531,29 @@ sgemm_status_t run(int variant, int64_t M, int64_t N, int64_t K, float alpha, co
   }
   if ((sg.a || sg.b) && gb300::launch_pack(copy_a, copy_b, stream) != cudaSuccess)
     return SGEMM_ERR_LAUNCH;
+  if (p.variant == SGEMM_VARIANT_SMALL) {
+    gb300::SmallArgs sa{};
+    sa.M = int(M);
+    sa.N = int(N);
+    sa.K = int(K);
+    sa.A = a_in;
+    sa.lda = lda_in;
+    sa.B = b_in;
+    sa.ldb = ldb_in;
+    sa.C = C;
+    sa.ldc = ldc;
+    sa.tiles_n = int(p.small_tiles_n);
+    sa.splits = p.splits;
+    sa.k_chunk = p.k_chunk;
+    sa.counters = static_cast<int32_t*>(ws);
+    sa.partials = ws ? reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes) : nullptr;
+    sa.scaled = scaled ? 1 : 0;
+    sa.alpha = alpha;
+    sa.beta = beta;
+    sa.c_scalar = operand_ok(C, ldc) ? 0 : 1;
+    return gb300::launch_small_kernel(sa, p.small_tiles, stream) == cudaSuccess ? SGEMM_OK
+                                                                               : SGEMM_ERR_LAUNCH;
+  }
   CUtensorMap tmap_a, tmap_b;
   st = encode_operands(ts, M, N, K, a_in, lda_in, b_in, ldb_in, &tmap_a, &tmap_b);
   if (st != SGEMM_OK) return st;
@@ -699,6 +785,7 @@ const char* sgemm_variant_name(int v) {
     case SGEMM_VARIANT_STREAMK_SMALL: return "streamk_small";
     case SGEMM_VARIANT_STAGED: return "staged";
     case SGEMM_VARIANT_SPECIALIZED: return "specialized";
+    case SGEMM_VARIANT_SMALL: return "small";
   }
   return "unknown";
 }

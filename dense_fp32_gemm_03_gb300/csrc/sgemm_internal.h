@@ -196,6 +196,31 @@ cudaError_t launch_tf32_pair_kernel(bool b_mn, const CUtensorMap& tmap_a, const 
                                     const Tf32Args& args, const Sched& sched, int pairs,
                                     cudaStream_t stream);
 
+// Small-product kernel (sgemm_small.cu): 64 x 64 tiles, K split into `splits`
+// shares of `k_chunk` (a multiple of 16) per tile; grid = tiles x splits.
+struct SmallArgs {
+  int32_t M, N, K;
+  const float* A;  // 16-byte aligned, lda a multiple of 4
+  int64_t lda;
+  const float* B;  // 16-byte aligned, ldb a multiple of 4
+  int64_t ldb;
+  float* C;
+  int64_t ldc;
+  int32_t tiles_n;
+  int32_t splits;
+  int32_t k_chunk;
+  float* partials;    // tiles x splits slots of 64 x 64 floats when splits > 1
+  int32_t* counters;  // one per tile, zero on entry and exit, when splits > 1
+  int32_t scaled;     // C = alpha * acc + beta * C (beta == 0 never reads C)
+  float alpha, beta;
+  int32_t c_scalar;   // C accessed 4 bytes at a time
+};
+struct SmallShape {
+  int bm, bn, bk;
+};
+SmallShape small_shape();
+cudaError_t launch_small_kernel(const SmallArgs& args, int64_t tiles, cudaStream_t stream);
+
 cudaError_t launch_guarded_kernel(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
                                   const float* B, int64_t ldb, float* C, int64_t ldc, int scaled,
                                   float alpha, float beta, cudaStream_t stream);

@@ -62,7 +62,8 @@ typedef enum {
   SGEMM_VARIANT_STREAMK_SMALL = 4, /* Stream-K schedule over 128x128 tiles */
   SGEMM_VARIANT_STAGED = 5,    /* any stride and alignment: unaligned A, B copied aligned first */
   SGEMM_VARIANT_SPECIALIZED = 6, /* Stream-K compiled for one exact shape (1024^3, 4096^3) */
-  SGEMM_VARIANT_COUNT = 7
+  SGEMM_VARIANT_SMALL = 7,     /* small products: 64x64 tiles, K split over CTAs, plain loads */
+  SGEMM_VARIANT_COUNT = 8
 } sgemm_variant_t;
 
 /*
@@ -104,7 +105,7 @@ sgemm_status_t sgemm_ex(int layout, int64_t M, int64_t N, int64_t K, float alpha
 
 /*
  * As sgemm() but forces `variant` (an sgemm_variant_t).  The four pipelined
- * variants (TILED, STREAMK, TILED_SMALL, STREAMK_SMALL) given operands they
+ * variants (TILED, STREAMK, TILED_SMALL, STREAMK_SMALL) and SMALL given operands they
  * cannot take (a base address that is not 16-byte aligned or a row stride
  * that is not a multiple of 4) return SGEMM_ERR_INVALID_VALUE without
  * launching.  GUARDED and STAGED take any operands; STAGED copies only the

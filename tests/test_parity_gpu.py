@@ -18,7 +18,7 @@ from parity import check_exact, check_within_bound
 
 pytestmark = pytest.mark.gpu
 
-FAST = [sg.TILED, sg.STREAMK, sg.TILED_SMALL, sg.STREAMK_SMALL]
+FAST = [sg.TILED, sg.STREAMK, sg.TILED_SMALL, sg.STREAMK_SMALL, sg.SMALL]
 ALL_VARIANTS = [sg.GUARDED, *FAST, sg.STAGED]
 SENTINEL = float.fromhex("0x1.dead00p+100")
 
