@@ -643,8 +643,11 @@ sgemm_status_t sgemm_tf32(int64_t M, int64_t N, int64_t K, const float* A, int64
   if (K == 0) {
     return gb300::launch_zero_fill(M, N, C, ldc, stream) == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
   }
-  // A goes to the tensor cores by TMA and C is stored 128 bits at a time.
-  if (!aligned16(A) || !aligned16(C) || lda % 4 != 0 || ldc % 4 != 0) return SGEMM_ERR_INVALID_VALUE;
+  // A goes to the tensor cores by TMA: an A that TMA cannot read in place is
+  // first copied into the workspace (rows padded to a multiple of 4 floats).
+  // A C that is not 16-byte aligned row by row is written 4 bytes at a time.
+  const bool a_copy = !operand_ok(A, lda);
+  const bool c_scalar = !operand_ok(C, ldc);
   // 128 x 256 x 32 tiles.  More tiles than resident CTAs: a persistent
   // Stream-K schedule (one CTA per SM) that splits the last partial wave over
   // K.  At most one wave: one tile per CTA, since reducing 128 KB partial
@@ -660,7 +663,8 @@ sgemm_status_t sgemm_tf32(int64_t M, int64_t N, int64_t K, const float* A, int64
   if (!lp.ok || lp.grid > kInt32Max ||
       lp.sc.sk_tiles * (pair ? 2 : 1) > kMaxSplitTiles)
     return SGEMM_ERR_UNSUPPORTED;
-  // Workspace: [counters][partial slots][B^T when B cannot be read in place].
+  // Workspace: [counters][partial slots][B^T when B cannot be read in place]
+  // [copy of A when A cannot be read in place].
   const size_t slot_bytes = size_t(bm) * bn * 4;
   const size_t partial_bytes = size_t(lp.slots) * slot_bytes;
   // B is read in place as an MN-major operand when TMA can address it;
@@ -669,11 +673,21 @@ sgemm_status_t sgemm_tf32(int64_t M, int64_t N, int64_t K, const float* A, int64
   const bool b_mn = operand_ok(B, ldb);
   const int64_t ldbt = (K + 3) / 4 * 4;
   const size_t bt_off = kCounterBytes + round_up(partial_bytes, 256);
-  const size_t ws_bytes =
+  const int64_t lda_copy = (K + 3) / 4 * 4;
+  const size_t a_off = round_up(b_mn ? kCounterBytes + partial_bytes : bt_off + size_t(N) * ldbt * 4, 256);
+  size_t ws_bytes =
       b_mn ? (partial_bytes ? kCounterBytes + partial_bytes : 0) : bt_off + size_t(N) * ldbt * 4;
+  if (a_copy) ws_bytes = a_off + size_t(M) * size_t(lda_copy) * 4;
   void* ws = nullptr;
   st = get_workspace_bytes(dev, stream, ws_bytes, &ws);
   if (st != SGEMM_OK) return st;
+  if (a_copy) {
+    float* a_dst = reinterpret_cast<float*>(static_cast<char*>(ws) + a_off);
+    const gb300::PackCopy copy{A, a_dst, M, K, lda, lda_copy};
+    if (gb300::launch_pack(copy, gb300::PackCopy{}, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    A = a_dst;
+    lda = lda_copy;
+  }
   const float* b_src = B;
   if (!b_mn) {
     float* Bt = reinterpret_cast<float*>(static_cast<char*>(ws) + bt_off);
@@ -721,6 +735,7 @@ sgemm_status_t sgemm_tf32(int64_t M, int64_t N, int64_t K, const float* A, int64
   args.partials = ws ? reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes) : nullptr;
   args.status = ds->status;
   args.wait_limit_ns = kDefaultWaitLimitNs;
+  args.c_scalar = c_scalar ? 1 : 0;
   const cudaError_t e =
       pair ? gb300::launch_tf32_pair_kernel(b_mn, tmap_a, tmap_b, args, lp.sc, int(lp.grid), stream)
            : gb300::launch_tf32_kernel(b_mn, tmap_a, tmap_b, args, lp.sc, int(lp.grid), stream);

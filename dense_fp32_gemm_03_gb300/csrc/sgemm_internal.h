@@ -175,6 +175,7 @@ struct Tf32Args {
   int32_t* counters;  // one arrival counter per split tile, zero on entry, zero on exit
   uint32_t* status;   // device status word
   uint64_t wait_limit_ns;
+  int32_t c_scalar;   // C is not 16-byte aligned row by row: 4-byte stores
 };
 // tmap_a: A (K fastest), box {32, 128}, 128-byte swizzle.  b_mn: tmap_b is B itself (N
 // fastest), box {32, 32}, 128-byte swizzle of 32-byte atoms; otherwise tmap_b is Bt (K

@@ -131,7 +131,7 @@ __device__ __forceinline__ void store_row32(const Tf32Args& args, int row, int c
                                             const float (&v)[32]) {
   if (row >= args.M) return;
   float* dst = args.C + int64_t(row) * args.ldc + col;
-  if (col + 32 <= args.N) {
+  if (col + 32 <= args.N && !args.c_scalar) {
 #pragma unroll
     for (int i = 0; i < 8; ++i)
       reinterpret_cast<float4*>(dst)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);

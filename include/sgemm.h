@@ -70,13 +70,17 @@ typedef enum {
  * C = A * B.  M, N, K >= 0; lda >= K, ldb >= N, ldc >= N (elements).
  * M == 0 or N == 0: nothing to do, SGEMM_OK.  K == 0: C is filled with zeros
  * (the empty sum).  Any stride and alignment is accepted.  The pipelined
- * kernels read A and B by TMA, which needs 16-byte-aligned base addresses and
- * row strides that are multiples of 4 floats.  An operand without that
- * property (for instance a contiguous matrix with an odd number of columns)
- * is either first copied into an aligned buffer in the workspace (the staged
- * variant; a C without it is then written with 4-byte stores) or the whole
- * product runs in the bounds-checked kernel, whichever the selector
- * estimates to be faster: the staged variant for all but small products.
+ * kernels read A and B by TMA, and the small-product kernel (SMALL, chosen
+ * for products up to roughly 512^3 and for thin or deep shapes whose tiles
+ * would leave SMs idle) with 128-bit loads: both need 16-byte-aligned base
+ * addresses and row strides that are multiples of 4 floats.  An operand
+ * without that property (for instance a contiguous matrix with an odd number
+ * of columns) is either first copied into an aligned buffer in the workspace
+ * (the staged variant; a C without it is then written with 4-byte stores) or
+ * the whole product runs in the bounds-checked kernel, whichever the
+ * selector estimates to be faster: the staged variant for all but very small
+ * products.  Every variant gives the same result on every call (summation
+ * orders are fixed); different variants may differ in rounding.
  */
 sgemm_status_t sgemm(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
                      const float *B, int64_t ldb, float *C, int64_t ldc, cudaStream_t stream);
@@ -153,12 +157,11 @@ size_t sgemm_workspace_size(int variant, int64_t M, int64_t N, int64_t K);
  * ("Beyond Kernel 7", section "The operation: GEMM and the precision of the
  * comparison"; "cuSgemm", Kernel 7).
  *
- * Same arguments and ownership as sgemm().  A and C must be 16-byte aligned
- * with lda and ldc multiples of 4 (else SGEMM_ERR_INVALID_VALUE); B may have
- * any stride.  A 16-byte-aligned B with ldb a multiple of 4 is read in place;
- * any other B is first copied transposed into the per-(device, stream)
- * workspace (N * round_up(K, 4) floats), which may grow with cudaMalloc as
- * for sgemm().
+ * Same arguments and ownership as sgemm(), and any stride and alignment.
+ * A 16-byte-aligned B with ldb a multiple of 4 is read in place; any other B
+ * is first copied transposed, and an A without that property copied as is,
+ * into the per-(device, stream) workspace, which may grow with cudaMalloc as
+ * for sgemm().  A C without it is written with 4-byte stores.
  */
 sgemm_status_t sgemm_tf32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
                           const float *B, int64_t ldb, float *C, int64_t ldc, cudaStream_t stream);

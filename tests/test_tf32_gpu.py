@@ -104,11 +104,24 @@ def test_tf32_ragged_shapes_and_k_tails(shape):
         assert bool(torch.isnan(C_big[:, N:]).all()), "wrote past N"
 
 
-def test_tf32_rejects_misaligned_a():
-    A = torch.ones(64, 66, device="cuda")[:, 1:]     # 4-byte offset
-    B = torch.ones(65, 64, device="cuda")
-    with pytest.raises(sg.SgemmError):
-        sg.sgemm_tf32(A, B)
+@pytest.mark.parametrize("shape", [(64, 64, 65), (300, 259, 201), (513, 771, 1027)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_tf32_any_alignment(shape):
+    """A starting 4 bytes off alignment with an odd stride (copied first), B with an odd
+    stride (transposed first), C starting 4 bytes off alignment (4-byte stores)."""
+    M, N, K = shape
+    A = workloads.matrix(M, K, "normal", 99, 0)
+    B = workloads.matrix(K, N, "normal", 99, 1)
+    ref, E = oracle.sgemm_f64(A, B)
+    bufA = torch.zeros(M * (K + 1) + 1, device="cuda")
+    dA = bufA[1:].as_strided((M, K), (K + 1, 1))
+    dA.copy_(A.cuda())
+    dB = B.cuda()                                    # ldb = N, odd for two of the shapes
+    big = torch.full((M * (N + 3) + 1,), float("nan"), device="cuda")
+    C = big[1:].as_strided((M, N), (N + 3, 1))
+    sg.sgemm_tf32(dA, dB, out=C)
+    torch.cuda.synchronize()
+    check_tf32(C.cpu().numpy(), ref, E, K, f"tf32 any alignment {shape}")
 
 
 @pytest.mark.parametrize("shape", [(256, 256, 256), (384, 520, 96), (129, 300, 77), (300, 33, 1029)],
