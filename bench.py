@@ -179,7 +179,7 @@ def ffma_peak_tflops(sms: int, mhz: float) -> float:
 
 
 # The files the tile kernel is compiled from, in a fixed order.
-KERNEL_SOURCES = ("sgemm_tile.cu", "sgemm_sched.cuh", "sgemm_device.cuh", "sgemm_internal.h")
+KERNEL_SOURCES = ("sgemm_tile.cu", "sgemm_sched.cuh", "sgemm_device.cuh", "sgemm_plan.h")
 
 
 def kernel_source_digest() -> str:

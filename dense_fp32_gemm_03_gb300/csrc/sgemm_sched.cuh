@@ -1,10 +1,10 @@
 // sgemm_sched.cuh -- device-side walk of the work decomposition (Sched in
-// sgemm_internal.h), shared by the FFMA tile kernel and the TF32 kernel.
+// sgemm_plan.h), shared by the FFMA tile kernel and the TF32 kernel.
 #pragma once
 
 #include <cstdint>
 
-#include "sgemm_internal.h"
+#include "sgemm_plan.h"
 
 namespace gb300 {
 

@@ -41,7 +41,7 @@
 #include <cuda_runtime.h>
 
 #include "sgemm_device.cuh"
-#include "sgemm_internal.h"
+#include "sgemm_plan.h"
 #include "sgemm_sched.cuh"
 
 namespace gb300 {
