@@ -10,7 +10,8 @@
 //
 // Structure: a persistent grid of one CTA per SM walks the same work
 // decomposition as the FFMA kernel (Sched: whole 128 x 256 tiles in full
-// waves, the tiles of the last partial wave split over K, Stream-K).
+// waves, the tiles of the last partial wave split over K, Stream-K), each
+// CTA its Stream-K share first (SkFirstIter).
 //  * A reaches shared memory by TMA in the canonical K-major layout with the
 //    128-byte swizzle that tcgen05.mma reads through its shared-memory
 //    descriptors.  B, row-major (N contiguous), is read as an MN-major
@@ -38,6 +39,56 @@
 
 namespace gb300 {
 namespace {
+
+// The TF32 kernels walk each CTA's (or CTA pair's) Stream-K share before its
+// whole tiles.  The epilogue warps then publish and add the split tiles'
+// partial sums while the tensor core computes whole tiles into the other
+// accumulator.  Walked last, as the FFMA kernel does, the share leaves its
+// reductions (latency-bound reads of the other sharers' partials) exposed
+// after the last MMA; walked first, only one whole tile's store is.
+struct SkFirstIter {
+  WorkIter w;
+  int dp_first;
+  bool sk_phase;
+
+  __device__ __forceinline__ void init(const Sched& sc, int cta) {
+    w.init(sc, cta);
+    dp_first = w.dp_next;
+    w.dp_next = sc.dp_tiles;  // no whole tile until the share is done
+    sk_phase = true;
+  }
+  __device__ __forceinline__ bool next(const Sched& sc, int ctas, Unit& u) {
+    if (sk_phase) {
+      if (w.next(sc, ctas, u)) return true;
+      sk_phase = false;
+      w.dp_next = dp_first;  // the share is exhausted: whole tiles only from here
+    }
+    return w.next(sc, ctas, u);
+  }
+};
+
+// KCursor over SkFirstIter: the k-tiles of all units in that order.
+struct SkFirstCursor {
+  SkFirstIter w;
+  Unit u;
+  int j;
+  int tm, tn;
+  bool valid;
+
+  __device__ __forceinline__ void init(const Sched& sc, int cta, int ctas) {
+    w.init(sc, cta);
+    j = 0;
+    valid = w.next(sc, ctas, u);
+    if (valid) tile_coords(sc, u.tile, tm, tn);
+  }
+  __device__ __forceinline__ void advance(const Sched& sc, int ctas) {
+    if (++j >= u.ke - u.kb) {
+      j = 0;
+      valid = w.next(sc, ctas, u);
+      if (valid) tile_coords(sc, u.tile, tm, tn);
+    }
+  }
+};
 
 constexpr int kTfBM = 128, kTfBN = 256, kTfBK = 32, kTfStages = 4, kTfThreads = 192;
 constexpr uint32_t kTfAStageBytes = kTfBM * kTfBK * 4;  // 16 KB
@@ -208,7 +259,7 @@ __global__ void __launch_bounds__(kTfThreads, 1)
       dev::tma_prefetch_desc(&tmap_a);
       dev::tma_prefetch_desc(&tmap_b);
     }
-    KCursor c;
+    SkFirstCursor c;
     c.init(sc, cta, ctas);
     uint32_t i = 0;
     for (; c.valid; ++i, c.advance(sc, ctas)) {
@@ -238,7 +289,7 @@ __global__ void __launch_bounds__(kTfThreads, 1)
   } else if (warp == 1) {
     // ---- MMA issuer: unit u accumulates into TMEM columns [256 (u mod 2), +256).
     // The whole warp walks the schedule and waits; one elected lane issues.
-    WorkIter w;
+    SkFirstIter w;
     w.init(sc, cta);
     Unit u;
     uint32_t it = 0, ui = 0;
@@ -285,7 +336,7 @@ __global__ void __launch_bounds__(kTfThreads, 1)
     const int row_local = 32 * q + lane;
     const int etid = threadIdx.x - 64;  // 0..127
     constexpr int64_t kSlotVec = int64_t(kTfBM) * kTfBN / 4;
-    WorkIter w;
+    SkFirstIter w;
     w.init(sc, cta);
     Unit u;
     uint32_t ui = 0;
@@ -559,7 +610,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTfThreads, 1)
       dev::tma_prefetch_desc(&tmap_a);
       dev::tma_prefetch_desc(&tmap_b);
     }
-    KCursor c;
+    SkFirstCursor c;
     c.init(sc, pair, pairs);
     uint32_t i = 0;
     for (; c.valid; ++i, c.advance(sc, pairs)) {
@@ -593,7 +644,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTfThreads, 1)
   } else if (warp == 1) {
     if (leader) {
       // ---- MMA issuer (leader only)
-      WorkIter w;
+      SkFirstIter w;
       w.init(sc, pair);
       Unit u;
       uint32_t it = 0, ui = 0;
@@ -638,7 +689,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTfThreads, 1)
     const int row_local = 32 * q + lane;
     const int etid = threadIdx.x - 64;
     constexpr int64_t kHalfVec = int64_t(kPrRows) * kPrBN / 4;  // one CTA's partial, in float4
-    WorkIter w;
+    SkFirstIter w;
     w.init(sc, pair);
     Unit u;
     uint32_t ui = 0;
