@@ -47,11 +47,13 @@ int tf32_pair_prepare();
 int tf32_pair_tile_m();
 int tf32_pair_tile_n();
 // tmap_b as for launch_tf32_kernel, except that a transposed Bt is read in boxes {32, 128};
-// `sched` is plan_launch over 256 x 256 x 32 tiles for `pairs` persistent pairs.  Split
-// tiles use two counters and two partial slots (one per CTA of the pair) each.
+// tmap_c: C (N fastest), box {32, 32}, 128-byte swizzle, used unless args.c_scalar (then
+// its contents are ignored).  `sched` is plan_launch over 256 x 256 x 32 tiles for `pairs`
+// persistent pairs.  Split tiles use two counters and two partial slots (one per CTA of
+// the pair) each.
 cudaError_t launch_tf32_pair_kernel(bool b_mn, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
-                                    const Tf32Args& args, const Sched& sched, int pairs,
-                                    cudaStream_t stream);
+                                    const CUtensorMap& tmap_c, const Tf32Args& args,
+                                    const Sched& sched, int pairs, cudaStream_t stream);
 
 // Small-product kernel (sgemm_small.cu): 64 x 64 tiles, K split into `splits`
 // shares of `k_chunk` (a multiple of 16) per tile; grid = tiles x splits.

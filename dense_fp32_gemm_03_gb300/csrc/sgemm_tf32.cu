@@ -479,8 +479,10 @@ constexpr uint32_t kPrBStageBytes = kPrCols * kPrBK * 4;    // 16 KB
 constexpr uint32_t kPrTmemCols = 512;
 constexpr int kPrAccBufs = int(kPrTmemCols / kPrBN);          // accumulators per CTA
 constexpr int kPrBarriers = 2 * kPrStages + 2 * 2 + 1;
+constexpr uint32_t kPrStagingBytes = kTfEpiWarps * 2 * 4096;  // CStager buffers of the epilogue warps
 constexpr size_t kPrSmem = 1024 + kPrStages * size_t(kPrAStageBytes + kPrBStageBytes) +
-                           kPrBarriers * 8 + 16;
+                           kPrStagingBytes + kPrBarriers * 8 + 16;
+static_assert(kPrSmem <= 232448, "shared memory per CTA");
 
 __host__ __device__ constexpr uint32_t pr_idesc(uint32_t b_mn) {
   return (1u << 4) | (2u << 7) | (2u << 10) | (0u << 15) | (b_mn << 16) |
@@ -546,16 +548,61 @@ __device__ __forceinline__ void remote_arrive(uint32_t bar_cluster_addr) {
                : "memory");
 }
 
+// Stores the box at element coordinates (x = column, y = row) of a 2-D tensor
+// map from shared memory as one bulk group of this thread.  Elements outside
+// the tensor are not written.  x must be a multiple of 4.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t x, int32_t y,
+                                             const void* src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(dev::smem_addr(src))
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// One epilogue warp's stores of C through shared memory: a 32 x 32 block
+// (row = lane) goes to one of two 4 KB buffers in the 128-byte swizzle that
+// TMA reads (16-byte chunk j of row r at j ^ (r mod 8), so the warp's
+// writes are free of bank conflicts), then out with one TMA store.  Every
+// 128-byte line of C is written whole, where row-per-lane stores would touch
+// 32 lines per instruction.
+struct CStager {
+  unsigned char* buf;  // two 4 KB buffers, 1024-byte aligned
+  uint32_t n;          // blocks stored so far
+
+  __device__ __forceinline__ void put(const CUtensorMap* map, int x, int y, const float (&v)[32],
+                                      int lane) {
+    unsigned char* b = buf + (n & 1u) * 4096u;
+    // The store that used this buffer two blocks ago has finished reading it.
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+    __syncwarp();
+    float4* row = reinterpret_cast<float4*>(b + lane * 128);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      row[i ^ (lane & 7)] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    dev::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) tma_store_2d(map, x, y, b);
+    ++n;
+  }
+  // Every store issued has completed (before shared memory is released).
+  __device__ __forceinline__ void drain(int lane) const {
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
+  }
+};
+
 template <bool B_MN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTfThreads, 1)
     tf32_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                     const Tf32Args args, const Sched sc) {
+                     const __grid_constant__ CUtensorMap tmap_c, const Tf32Args args, const Sched sc) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = dev::smem_addr(smem_raw);
   unsigned char* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   unsigned char* sA = smem;
   unsigned char* sB = smem + kPrStages * kPrAStageBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kPrStages * kPrBStageBytes);  // used in the leader
+  unsigned char* sC = sB + kPrStages * kPrBStageBytes;  // epilogue staging (1024-byte aligned)
+  uint64_t* full = reinterpret_cast<uint64_t*>(sC + kPrStagingBytes);  // used in the leader
   uint64_t* empty = full + kPrStages;
   uint64_t* acc_full = empty + kPrStages;  // [2]
   uint64_t* acc_empty = acc_full + 2;      // [2], used in the leader: 4 warps x 2 CTAs arrive
@@ -689,6 +736,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTfThreads, 1)
     const int row_local = 32 * q + lane;
     const int etid = threadIdx.x - 64;
     constexpr int64_t kHalfVec = int64_t(kPrRows) * kPrBN / 4;  // one CTA's partial, in float4
+    // C aligned for TMA: stores through shared memory (CStager); otherwise
+    // row by row, 4 bytes at a time.  A TMA store clips a box at the right
+    // edge of C only to 16-byte granules (measured on GB300: with N not a
+    // multiple of 4 it wrote the columns up to the next multiple of 4), so
+    // the block holding column N - 1 of such a C is stored row by row.
+    const bool tma_c = !args.c_scalar;
+    const bool tma_edge = (args.N & 3) == 0;  // a TMA store may cross column N
+    CStager stager{sC + q * 8192, 0};
+    if (tma_c && lane == 0) dev::tma_prefetch_desc(&tmap_c);
     SkFirstIter w;
     w.init(sc, pair);
     Unit u;
@@ -700,14 +756,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTfThreads, 1)
       int tm, tn;
       tile_coords(sc, u.tile, tm, tn);
       const int row = tm * kPrBM + int(rank) * kPrRows + row_local, n0 = tn * kPrBN;
+      const int row0 = row - lane;  // first row of this warp's 32
       const uint32_t taddr = tmem + b * kPrBN + (uint32_t(32 * q) << 16);
-      const bool ok = !*s_abort;
+      const bool ok = __shfl_sync(0xffffffffu, !*s_abort ? 1 : 0, 0) != 0;  // warp-uniform
+      // Row `row`, columns col .. col + 31 of C.
+      auto emit = [&](int col, const float(&v)[32]) {
+        if (tma_c && (tma_edge || col + 32 <= args.N))
+          stager.put(&tmap_c, col, row0, v, lane);
+        else
+          store_row32(args, row, col, v);
+      };
       if (u.t_sk < 0 || (u.kb == 0 && u.ke == sc.iters_per_tile)) {
 #pragma unroll 1
         for (int c = 0; c < kPrBN; c += 32) {
           uint32_t r[32];
           tc_ld32(taddr + uint32_t(c), r);
-          if (ok) store_row32(args, row, n0 + c, reinterpret_cast<const float(&)[32]>(r));
+          if (ok) emit(n0 + c, reinterpret_cast<const float(&)[32]>(r));
         }
       } else {
         // Split tile, per CTA half: counters[2 t + rank], slot 2 (t + pair) + rank.
@@ -784,8 +848,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTfThreads, 1)
                 sum[4 * v + 3] += x[v].w;
               }
             }
-            store_row32(args, row, n0 + c, reinterpret_cast<const float(&)[32]>(sum[0]));
-            store_row32(args, row, n0 + c + 32, reinterpret_cast<const float(&)[32]>(sum[32]));
+            emit(n0 + c, reinterpret_cast<const float(&)[32]>(sum[0]));
+            emit(n0 + c + 32, reinterpret_cast<const float(&)[32]>(sum[32]));
           }
           if (etid == 0) *counter = 0;
         }
@@ -795,6 +859,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTfThreads, 1)
       if (lane == 0) remote_arrive(peer_addr(&acc_empty[b], 0));
       ++ui;
     }
+    if (tma_c) stager.drain(lane);
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
@@ -935,12 +1000,12 @@ int tf32_pair_tile_m() { return kPrBM; }
 int tf32_pair_tile_n() { return kPrBN; }
 
 cudaError_t launch_tf32_pair_kernel(bool b_mn, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
-                                    const Tf32Args& args, const Sched& sched, int pairs,
-                                    cudaStream_t stream) {
+                                    const CUtensorMap& tmap_c, const Tf32Args& args, const Sched& sched,
+                                    int pairs, cudaStream_t stream) {
   if (b_mn)
-    tf32_pair_kernel<true><<<2 * pairs, kTfThreads, kPrSmem, stream>>>(tmap_a, tmap_b, args, sched);
+    tf32_pair_kernel<true><<<2 * pairs, kTfThreads, kPrSmem, stream>>>(tmap_a, tmap_b, tmap_c, args, sched);
   else
-    tf32_pair_kernel<false><<<2 * pairs, kTfThreads, kPrSmem, stream>>>(tmap_a, tmap_b, args, sched);
+    tf32_pair_kernel<false><<<2 * pairs, kTfThreads, kPrSmem, stream>>>(tmap_a, tmap_b, tmap_c, args, sched);
   return cudaGetLastError();
 }
 

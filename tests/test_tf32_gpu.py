@@ -152,6 +152,28 @@ def test_tf32_b_in_place_and_transposed(shape):
         check_tf32(C.cpu().numpy(), ref, E, K, f"tf32 {shape} B {what}")
 
 
+@pytest.mark.parametrize("shape", [(200, 260, 64), (200, 261, 64), (300, 518, 96), (257, 515, 40),
+                                   (513, 1024, 48), (1029, 2051, 64), (2600, 2301, 256)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_tf32_edges_leave_neighbours_untouched(shape):
+    """C inside a larger NaN-filled buffer (rows below it, columns right of it): stores at
+    the M and N edges (TMA boxes clipped by the hardware, or row stores where N is not a
+    multiple of 4) write C and nothing else, on integer inputs that must be exact."""
+    M, N, K = shape
+    A = workloads.matrix(M, K, "int8range", 71 + N, 0)
+    B = workloads.matrix(K, N, "int8range", 71 + N, 1)
+    ref, E = oracle.sgemm_f64(A, B)
+    assert E.max() < 2 ** 24
+    ldc = (N + 3) // 4 * 4 + 8                   # 8 or more canary columns on the right
+    big = torch.full((M + 40, ldc), float("nan"), device="cuda")
+    C = big[:M, :N]
+    sg.sgemm_tf32(A.cuda(), B.cuda(), out=C)
+    torch.cuda.synchronize()
+    check_exact(C.cpu().numpy(), ref, f"tf32 edges {shape}")
+    assert bool(torch.isnan(big[:M, N:]).all()), "wrote right of column N - 1"
+    assert bool(torch.isnan(big[M:]).all()), "wrote below row M - 1"
+
+
 def test_tf32_integers_exact_through_both_b_paths():
     M, N, K = 256, 512, 384
     A = workloads.matrix(M, K, "int8range", 95, 0)
