@@ -726,10 +726,10 @@ sgemm_status_t sgemm_tf32(int64_t M, int64_t N, int64_t K, const float* A, int64
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return SGEMM_ERR_LAUNCH;
   }
-  // C for the pair kernel's TMA stores: boxes of 32 columns x 32 rows, 128-byte swizzle.
+  // C for the kernels' TMA stores: boxes of 32 columns x 32 rows, 128-byte swizzle.
   CUtensorMap tmap_c;
   std::memset(&tmap_c, 0, sizeof(tmap_c));
-  if (pair && !c_scalar) {
+  if (!c_scalar) {
     const cuuint64_t dims[2] = {cuuint64_t(N), cuuint64_t(M)};
     const cuuint64_t strides[1] = {cuuint64_t(ldc) * 4};
     const cuuint32_t box[2] = {32, 32};
@@ -751,7 +751,7 @@ sgemm_status_t sgemm_tf32(int64_t M, int64_t N, int64_t K, const float* A, int64
   const cudaError_t e =
       pair ? gb300::launch_tf32_pair_kernel(b_mn, tmap_a, tmap_b, tmap_c, args, lp.sc, int(lp.grid),
                                              stream)
-           : gb300::launch_tf32_kernel(b_mn, tmap_a, tmap_b, args, lp.sc, int(lp.grid), stream);
+           : gb300::launch_tf32_kernel(b_mn, tmap_a, tmap_b, tmap_c, args, lp.sc, int(lp.grid), stream);
   return e == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
 }
 

@@ -35,20 +35,20 @@ struct Tf32Args {
 };
 // tmap_a: A (K fastest), box {32, 128}, 128-byte swizzle.  b_mn: tmap_b is B itself (N
 // fastest), box {32, 32}, 128-byte swizzle of 32-byte atoms; otherwise tmap_b is Bt (K
-// fastest), box {32, 256}, 128-byte swizzle.  `sched` is plan_launch over 128 x 256 x 32
-// tiles for `grid` persistent CTAs.
+// fastest), box {32, 256}, 128-byte swizzle.  tmap_c: C (N fastest), box {32, 32},
+// 128-byte swizzle, used unless args.c_scalar (then its contents are ignored).  `sched` is
+// plan_launch over 128 x 256 x 32 tiles for `grid` persistent CTAs.
 cudaError_t launch_tf32_kernel(bool b_mn, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
-                               const Tf32Args& args, const Sched& sched, int grid,
-                               cudaStream_t stream);
+                               const CUtensorMap& tmap_c, const Tf32Args& args, const Sched& sched,
+                               int grid, cudaStream_t stream);
 
 // CTA-pair TF32 kernel (tcgen05.mma.cta_group::2): 256 x 256 tiles per pair of SMs.  Returns
 // the CTA pairs that can run at once, or <= 0 if none.
 int tf32_pair_prepare();
 int tf32_pair_tile_m();
 int tf32_pair_tile_n();
-// tmap_b as for launch_tf32_kernel, except that a transposed Bt is read in boxes {32, 128};
-// tmap_c: C (N fastest), box {32, 32}, 128-byte swizzle, used unless args.c_scalar (then
-// its contents are ignored).  `sched` is plan_launch over 256 x 256 x 32 tiles for `pairs`
+// tmap_b and tmap_c as for launch_tf32_kernel, except that a transposed Bt is read in
+// boxes {32, 128}.  `sched` is plan_launch over 256 x 256 x 32 tiles for `pairs`
 // persistent pairs.  Split tiles use two counters and two partial slots (one per CTA of
 // the pair) each.
 cudaError_t launch_tf32_pair_kernel(bool b_mn, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,

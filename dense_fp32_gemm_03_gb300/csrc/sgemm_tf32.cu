@@ -97,8 +97,10 @@ constexpr uint32_t kTfTmemCols = 2 * kTfBN;             // two accumulators of 1
 constexpr int kTfEpiWarps = 4;                          // warps 2..5
 constexpr int kTfEpiThreads = 32 * kTfEpiWarps;
 constexpr int kTfBarriers = 2 * kTfStages + 5;          // full, empty, acc_full[2], acc_empty[2], drain
+constexpr uint32_t kTfStagingBytes = kTfEpiWarps * 2 * 4096;  // CStager buffers of the epilogue warps
 constexpr size_t kTfSmem = 1024 /* alignment slack */ + kTfStages * size_t(kTfAStageBytes + kTfBStageBytes) +
-                           kTfBarriers * 8 + 16;
+                           kTfStagingBytes + kTfBarriers * 8 + 16;
+static_assert(kTfSmem <= 232448, "shared memory per CTA");
 constexpr uint32_t kStatusTimeout = 3;
 
 // Instruction descriptor of tcgen05.mma kind::tf32: FP32 accumulator, TF32 A
@@ -193,19 +195,64 @@ __device__ __forceinline__ void store_row32(const Tf32Args& args, int row, int c
   }
 }
 
+// Stores the box at element coordinates (x = column, y = row) of a 2-D tensor
+// map from shared memory as one bulk group of this thread.  Elements outside
+// the tensor are not written.  x must be a multiple of 4.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t x, int32_t y,
+                                             const void* src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(dev::smem_addr(src))
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// One epilogue warp's stores of C through shared memory: a 32 x 32 block
+// (row = lane) goes to one of two 4 KB buffers in the 128-byte swizzle that
+// TMA reads (16-byte chunk j of row r at j ^ (r mod 8), so the warp's
+// writes are free of bank conflicts), then out with one TMA store.  Every
+// 128-byte line of C is written whole, where row-per-lane stores would touch
+// 32 lines per instruction.
+struct CStager {
+  unsigned char* buf;  // two 4 KB buffers, 1024-byte aligned
+  uint32_t n;          // blocks stored so far
+
+  __device__ __forceinline__ void put(const CUtensorMap* map, int x, int y, const float (&v)[32],
+                                      int lane) {
+    unsigned char* b = buf + (n & 1u) * 4096u;
+    // The store that used this buffer two blocks ago has finished reading it.
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+    __syncwarp();
+    float4* row = reinterpret_cast<float4*>(b + lane * 128);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      row[i ^ (lane & 7)] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    dev::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) tma_store_2d(map, x, y, b);
+    ++n;
+  }
+  // Every store issued has completed (before shared memory is released).
+  __device__ __forceinline__ void drain(int lane) const {
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
+  }
+};
+
 // B_MN: B is read in place as an MN-major operand (tmap_b: B, N fastest, box
 // 32 x 32); otherwise tmap_b holds B^T (K fastest, box 32 x 256) like A.
 template <bool B_MN>
 __global__ void __launch_bounds__(kTfThreads, 1)
     tf32_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                const Tf32Args args, const Sched sc) {
+                const __grid_constant__ CUtensorMap tmap_c, const Tf32Args args, const Sched sc) {
   extern __shared__ unsigned char smem_raw[];
   // Stages must sit on 1024-byte boundaries (the 128-byte swizzle period).
   const uint32_t raw = dev::smem_addr(smem_raw);
   unsigned char* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   unsigned char* sA = smem;
   unsigned char* sB = smem + kTfStages * kTfAStageBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kTfStages * kTfBStageBytes);
+  unsigned char* sC = sB + kTfStages * kTfBStageBytes;  // epilogue staging (1024-byte aligned)
+  uint64_t* full = reinterpret_cast<uint64_t*>(sC + kTfStagingBytes);
   uint64_t* empty = full + kTfStages;
   uint64_t* acc_full = empty + kTfStages;  // [2] accumulator b holds a finished unit
   uint64_t* acc_empty = acc_full + 2;      // [2] the epilogue has read accumulator b
@@ -336,6 +383,12 @@ __global__ void __launch_bounds__(kTfThreads, 1)
     const int row_local = 32 * q + lane;
     const int etid = threadIdx.x - 64;  // 0..127
     constexpr int64_t kSlotVec = int64_t(kTfBM) * kTfBN / 4;
+    // C through shared memory and TMA where TMA can address it (CStager;
+    // the block over a right edge that is not 16-byte aligned row by row).
+    const bool tma_c = !args.c_scalar;
+    const bool tma_edge = (args.N & 3) == 0;
+    CStager stager{sC + q * 8192, 0};
+    if (tma_c && lane == 0) dev::tma_prefetch_desc(&tmap_c);
     SkFirstIter w;
     w.init(sc, cta);
     Unit u;
@@ -348,13 +401,20 @@ __global__ void __launch_bounds__(kTfThreads, 1)
       tile_coords(sc, u.tile, tm, tn);
       const int row = tm * kTfBM + row_local, n0 = tn * kTfBN;
       const uint32_t taddr = tmem + b * kTfBN + (uint32_t(32 * q) << 16);
-      const bool ok = !*s_abort;
+      const bool ok = __shfl_sync(0xffffffffu, !*s_abort ? 1 : 0, 0) != 0;  // warp-uniform
+      // Row `row`, columns col .. col + 31 of C.
+      auto emit = [&](int col, const float(&v)[32]) {
+        if (tma_c && (tma_edge || col + 32 <= args.N))
+          stager.put(&tmap_c, col, row - lane, v, lane);
+        else
+          store_row32(args, row, col, v);
+      };
       if (u.t_sk < 0 || (u.kb == 0 && u.ke == sc.iters_per_tile)) {
 #pragma unroll 1
         for (int c = 0; c < kTfBN; c += 32) {
           uint32_t r[32];
           tc_ld32(taddr + uint32_t(c), r);
-          if (ok) store_row32(args, row, n0 + c, reinterpret_cast<const float(&)[32]>(r));
+          if (ok) emit(n0 + c, reinterpret_cast<const float(&)[32]>(r));
         }
       } else {
         // Split tile, as in the FFMA kernel: the sharers publish their partial
@@ -435,8 +495,8 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                 sum[4 * v + 3] += x[v].w;
               }
             }
-            store_row32(args, row, n0 + c, reinterpret_cast<const float(&)[32]>(sum[0]));
-            store_row32(args, row, n0 + c + 32, reinterpret_cast<const float(&)[32]>(sum[32]));
+            emit(n0 + c, reinterpret_cast<const float(&)[32]>(sum[0]));
+            emit(n0 + c + 32, reinterpret_cast<const float(&)[32]>(sum[32]));
           }
           if (etid == 0) args.counters[u.t_sk] = 0;
         }
@@ -447,6 +507,7 @@ __global__ void __launch_bounds__(kTfThreads, 1)
       if (lane == 0) dev::mbar_arrive(&acc_empty[b]);
       ++ui;
     }
+    if (tma_c) stager.drain(lane);
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
@@ -547,50 +608,6 @@ __device__ __forceinline__ void remote_arrive(uint32_t bar_cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr)
                : "memory");
 }
-
-// Stores the box at element coordinates (x = column, y = row) of a 2-D tensor
-// map from shared memory as one bulk group of this thread.  Elements outside
-// the tensor are not written.  x must be a multiple of 4.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t x, int32_t y,
-                                             const void* src) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y), "r"(dev::smem_addr(src))
-               : "memory");
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-// One epilogue warp's stores of C through shared memory: a 32 x 32 block
-// (row = lane) goes to one of two 4 KB buffers in the 128-byte swizzle that
-// TMA reads (16-byte chunk j of row r at j ^ (r mod 8), so the warp's
-// writes are free of bank conflicts), then out with one TMA store.  Every
-// 128-byte line of C is written whole, where row-per-lane stores would touch
-// 32 lines per instruction.
-struct CStager {
-  unsigned char* buf;  // two 4 KB buffers, 1024-byte aligned
-  uint32_t n;          // blocks stored so far
-
-  __device__ __forceinline__ void put(const CUtensorMap* map, int x, int y, const float (&v)[32],
-                                      int lane) {
-    unsigned char* b = buf + (n & 1u) * 4096u;
-    // The store that used this buffer two blocks ago has finished reading it.
-    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-    __syncwarp();
-    float4* row = reinterpret_cast<float4*>(b + lane * 128);
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      row[i ^ (lane & 7)] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-    dev::fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) tma_store_2d(map, x, y, b);
-    ++n;
-  }
-  // Every store issued has completed (before shared memory is released).
-  __device__ __forceinline__ void drain(int lane) const {
-    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-    __syncwarp();
-  }
-};
 
 template <bool B_MN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTfThreads, 1)
@@ -1010,12 +1027,12 @@ cudaError_t launch_tf32_pair_kernel(bool b_mn, const CUtensorMap& tmap_a, const 
 }
 
 cudaError_t launch_tf32_kernel(bool b_mn, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
-                               const Tf32Args& args, const Sched& sched, int grid,
-                               cudaStream_t stream) {
+                               const CUtensorMap& tmap_c, const Tf32Args& args, const Sched& sched,
+                               int grid, cudaStream_t stream) {
   if (b_mn)
-    tf32_kernel<true><<<grid, kTfThreads, kTfSmem, stream>>>(tmap_a, tmap_b, args, sched);
+    tf32_kernel<true><<<grid, kTfThreads, kTfSmem, stream>>>(tmap_a, tmap_b, tmap_c, args, sched);
   else
-    tf32_kernel<false><<<grid, kTfThreads, kTfSmem, stream>>>(tmap_a, tmap_b, args, sched);
+    tf32_kernel<false><<<grid, kTfThreads, kTfSmem, stream>>>(tmap_a, tmap_b, tmap_c, args, sched);
   return cudaGetLastError();
 }
 

@@ -221,13 +221,25 @@ for (M, N, K) in [(256, 512, 384), (1000, 1000, 2048), (4096, 4096, 512)]:
     assert E.max() < 2 ** 24
     got = C[r.cuda(), c.cuda()].cpu().numpy().astype(np.float64)
     assert np.array_equal(got, ref), (M, N, K)
+# C inside NaN canaries (rows below, columns right; N % 4 = 1, 3, 1).
+for (M, N, K) in [(200, 261, 64), (1029, 2051, 64), (2600, 2301, 256)]:
+    A = workloads.matrix(M, K, "int8range", 71 + N, 0)
+    B = workloads.matrix(K, N, "int8range", 71 + N, 1)
+    ref, E = oracle.sgemm_f64(A, B)
+    ldc = (N + 3) // 4 * 4 + 8
+    big = torch.full((M + 40, ldc), float("nan"), device="cuda")
+    sg.sgemm_tf32(A.cuda(), B.cuda(), out=big[:M, :N])
+    torch.cuda.synchronize()
+    assert np.array_equal(big[:M, :N].cpu().numpy().astype(np.float64), ref), (M, N, K)
+    assert bool(torch.isnan(big[:M, N:]).all()) and bool(torch.isnan(big[M:]).all()), (M, N, K)
 assert sg.query_device_status() == (0, 0)
 print("single-SM path ok")
 """
 
 
 def test_tf32_single_sm_kernel_in_a_subprocess():
-    """The single-SM kernel (used where no CTA pair fits) stays exact on integers."""
+    """The single-SM kernel (used where no CTA pair fits) stays exact on integers and writes
+    nothing outside C."""
     import os
     import subprocess
     import sys
