@@ -40,6 +40,9 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <tuple>
+#include <utility>
+
 #include "sgemm_device.cuh"
 #include "sgemm_plan.h"
 #include "sgemm_sched.cuh"
@@ -526,11 +529,64 @@ int prepare() {
   return blocks;
 }
 
-// The size-specialized instances: configuration id, M, N, K.
-using Spec4096 = Cfg0;  // configuration 0, the default for large shapes
-using Spec1024 = Cfg3;  // configuration 3, the default for small shapes
-constexpr SpecShape kSpecShapes[] = {{0, 4096, 4096, 4096}, {3, 1024, 1024, 1024}};
-constexpr int kSpecCount = int(sizeof(kSpecShapes) / sizeof(kSpecShapes[0]));
+// The size-specialized instances: configuration id and M = N = K.  The
+// square sizes of the measured sweep that run the tile kernel (768^3 and
+// 1024^3 on 128 x 128 tiles, 1536^3, 2048^3 and 4096^3 on 128 x 256; 512^3
+// and below run the small-product kernel).
+template <int ID>
+struct CfgById;
+template <>
+struct CfgById<0> {
+  using type = Cfg0;
+};
+template <>
+struct CfgById<3> {
+  using type = Cfg3;
+};
+
+template <int ID, int M, int N, int K>
+struct SpecInst {
+  using T = typename CfgById<ID>::type;
+  static SpecShape shape() { return SpecShape{ID, M, N, K}; }
+  static bool prepare() {
+    return cudaFuncSetAttribute(tile_kernel<T, false, M, N, K>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                int(T::kSmem)) == cudaSuccess;
+  }
+  static void launch(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const GemmArgs& args,
+                     const Sched& sched, int grid, cudaStream_t stream) {
+    tile_kernel<T, false, M, N, K><<<grid, T::NT, T::kSmem, stream>>>(tmap_a, tmap_b, args, sched);
+  }
+};
+
+using SpecList = std::tuple<SpecInst<0, 4096, 4096, 4096>, SpecInst<3, 1024, 1024, 1024>,
+                            SpecInst<3, 768, 768, 768>, SpecInst<0, 1536, 1536, 1536>,
+                            SpecInst<0, 2048, 2048, 2048>>;
+constexpr int kSpecCount = int(std::tuple_size<SpecList>::value);
+using SpecIndex = std::make_index_sequence<std::tuple_size<SpecList>::value>;
+
+template <size_t... I>
+SpecShape spec_shape_at(int i, std::index_sequence<I...>) {
+  SpecShape out{-1, 0, 0, 0};
+  ((int(I) == i ? (out = std::tuple_element_t<I, SpecList>::shape(), true) : false) || ...);
+  return out;
+}
+
+template <size_t... I>
+bool spec_prepare_all(std::index_sequence<I...>) {
+  return (std::tuple_element_t<I, SpecList>::prepare() && ...);
+}
+
+template <size_t... I>
+bool spec_launch_at(int i, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                    const GemmArgs& args, const Sched& sched, int grid, cudaStream_t stream,
+                    std::index_sequence<I...>) {
+  return ((int(I) == i
+               ? (std::tuple_element_t<I, SpecList>::launch(tmap_a, tmap_b, args, sched, grid, stream),
+                  true)
+               : false) ||
+          ...);
+}
 
 template <class T>
 TileShape shape_of() {
@@ -550,34 +606,15 @@ int tile_kernel_prepare(TileConfig cfg) {
 
 int specialized_count() { return kSpecCount; }
 
-SpecShape specialized_shape(int i) { return kSpecShapes[i]; }
+SpecShape specialized_shape(int i) { return spec_shape_at(i, SpecIndex{}); }
 
-int specialized_prepare() {
-  if (cudaFuncSetAttribute(tile_kernel<Spec4096, false, 4096, 4096, 4096>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           int(Spec4096::kSmem)) != cudaSuccess ||
-      cudaFuncSetAttribute(tile_kernel<Spec1024, false, 1024, 1024, 1024>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           int(Spec1024::kSmem)) != cudaSuccess)
-    return -1;
-  return 0;
-}
+int specialized_prepare() { return spec_prepare_all(SpecIndex{}) ? 0 : -1; }
 
 cudaError_t launch_specialized(int i, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                                const GemmArgs& args, const Sched& sched, int grid,
                                cudaStream_t stream) {
-  switch (i) {
-    case 0:
-      tile_kernel<Spec4096, false, 4096, 4096, 4096>
-          <<<grid, Spec4096::NT, Spec4096::kSmem, stream>>>(tmap_a, tmap_b, args, sched);
-      break;
-    case 1:
-      tile_kernel<Spec1024, false, 1024, 1024, 1024>
-          <<<grid, Spec1024::NT, Spec1024::kSmem, stream>>>(tmap_a, tmap_b, args, sched);
-      break;
-    default:
-      return cudaErrorInvalidValue;
-  }
+  if (!spec_launch_at(i, tmap_a, tmap_b, args, sched, grid, stream, SpecIndex{}))
+    return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 

@@ -1,4 +1,4 @@
-"""GPU parity of the size-specialized instances (M = N = K = 1024 and 4096).
+"""GPU parity of the size-specialized instances (M = N = K = 768, 1024, 1536, 2048, 4096).
 
 The specialized instance runs the same Stream-K schedule as the generic
 kernel with the shape compiled in, so its output must equal the generic
@@ -30,9 +30,16 @@ def _built():
     assert st == 0, f"device status {st} (site {site}) left after the module"
 
 
-@pytest.mark.parametrize("w,generic", [(workloads.SQUARE_1024, sg.STREAMK_SMALL),
+def _sweep(n):
+    return next(w for w in workloads.SWEEP if w.M == n)
+
+
+@pytest.mark.parametrize("w,generic", [(_sweep(768), sg.STREAMK_SMALL),
+                                       (workloads.SQUARE_1024, sg.STREAMK_SMALL),
+                                       (_sweep(1536), sg.STREAMK),
+                                       (_sweep(2048), sg.STREAMK),
                                        (workloads.SQUARE_4096, sg.STREAMK)],
-                         ids=["1024", "4096"])
+                         ids=["768", "1024", "1536", "2048", "4096"])
 def test_selected_and_bit_identical_to_generic(w, generic):
     A, B = (x.cuda() for x in workloads.operands(w))
     C_spec = torch.full((w.M, w.N), float("nan"), device="cuda")
@@ -52,6 +59,28 @@ def test_1024_full_compare():
     C = sg.sgemm(A.cuda(), B.cuda(), variant=sg.SPECIALIZED)
     torch.cuda.synchronize()
     check_within_bound(C.cpu().numpy(), ref, E, w.K, "1024^3 specialized")
+
+
+def test_768_full_compare():
+    w = _sweep(768)
+    A, B = workloads.operands(w)
+    ref, E = oracle.sgemm_f64(A, B)
+    C = sg.sgemm(A.cuda(), B.cuda(), variant=sg.SPECIALIZED)
+    torch.cuda.synchronize()
+    check_within_bound(C.cpu().numpy(), ref, E, w.K, "768^3 specialized")
+
+
+@pytest.mark.parametrize("n", [1536, 2048])
+def test_sweep_sizes_sampled_and_last_tile_row(n):
+    w = _sweep(n)
+    A, B = workloads.operands(w)
+    C = sg.sgemm(A.cuda(), B.cuda(), variant=sg.SPECIALIZED).cpu().numpy()
+    r, c = workloads.sample_indices(w.M, w.N, 4096, w.seed)
+    ref, E = oracle.sgemm_entries_f64(A, B, r.numpy(), c.numpy())
+    check_within_bound(C[r.numpy(), c.numpy()], ref, E, w.K, f"{n}^3 specialized (sampled)")
+    rows = slice(n - 128, n)
+    ref, E = oracle.sgemm_f64(A[rows], B)
+    check_within_bound(C[rows], ref, E, w.K, f"{n}^3 specialized, last tile row")
 
 
 def test_4096_sampled_and_row_block():
