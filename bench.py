@@ -8,9 +8,10 @@ before every timed step by writing a buffer twice the L2 size, and every step
 is timed with CUDA events on the launching stream (the flush is outside the
 events), as in "Beyond Kernel 7", section "The confirmed result".
 Throughput counts 2*M*N*K operations per call (an FFMA counts as two).
-At 1024^3 and 4096^3 the selector takes the size-specialized kernel instance
-(shape and schedule compiled in); the best generic variant is timed on the
-same protocol and reported beside it under ``generic``.
+At 1024^3 and 4096^3 (and the sweep's 768^3, 1536^3 and 2048^3) the selector
+takes a size-specialized kernel instance (shape and schedule compiled in); the
+best generic variant is timed on the same protocol and reported beside it
+under ``generic``.
 
 Also reported: the same metric end to end through the C ABI with pinned host
 buffers (host-to-device copies of A and B and the device-to-host copy of C

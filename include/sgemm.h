@@ -61,7 +61,7 @@ typedef enum {
   SGEMM_VARIANT_TILED_SMALL = 3,   /* pipelined 128x128 tiles, one output tile per CTA */
   SGEMM_VARIANT_STREAMK_SMALL = 4, /* Stream-K schedule over 128x128 tiles */
   SGEMM_VARIANT_STAGED = 5,    /* any stride and alignment: unaligned A, B copied aligned first */
-  SGEMM_VARIANT_SPECIALIZED = 6, /* Stream-K compiled for one exact shape (1024^3, 4096^3) */
+  SGEMM_VARIANT_SPECIALIZED = 6, /* Stream-K compiled for one exact shape (768^3 ... 4096^3) */
   SGEMM_VARIANT_SMALL = 7,     /* small products: 64x64 tiles, K split over CTAs, plain loads */
   SGEMM_VARIANT_COUNT = 8
 } sgemm_variant_t;
