@@ -5,9 +5,9 @@
 // tensor-map descriptors.  Here a CTA of 128 threads computes a 64 x 64
 // tile over one share of K ("2D Block Tiling ...", section 4: register
 // outer products of 4 x 8 per thread, "Beyond Kernel 7", section "Kernel
-// 6": warp tiling), with plain 128-bit loads staged through registers into
-// double-buffered shared memory (the prefetch of "Beyond Kernel 7",
-// section "Kernel 8").  K is split so that the grid fills the GPU; the
+// 6": warp tiling), fed by asynchronous 16-byte copies (cp.async) into a
+// four-stage shared-memory ring (the multi-stage copy pipeline of "Beyond
+// Kernel 7", section "Kernel 8").  K is split so that the grid fills the GPU; the
 // shares of a tile publish their partial sums and the last to arrive adds
 // them in share order, so the result is the same whoever finishes last.
 #include <cuda_runtime.h>
@@ -21,68 +21,57 @@ namespace {
 constexpr int kSmBM = 64, kSmBN = 64, kSmBK = 16, kSmThreads = 128;
 constexpr int kSmVec = kSmBM * kSmBN / 4 / kSmThreads;  // float4 outputs per thread: 8
 
-// A k-slice of A (64 rows x 16) and of B (16 x 64 columns) held in registers
-// between its global loads and its shared-memory stores.
-struct Slice {
-  float4 a[2];
-  float4 b[2];
-};
+constexpr int kSmStages = 4;  // k-slices in the shared-memory ring (three in flight)
 
-// 128-bit load of row[0..3], columns col..col+3 that lie below `end`, zeros elsewhere.
-__device__ __forceinline__ float4 load4(const float* row, int64_t col, int64_t end) {
-  if (col + 3 < end) return __ldg(reinterpret_cast<const float4*>(row + col));
-  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (col + 0 < end) v.x = __ldg(row + col);
-  if (col + 1 < end) v.y = __ldg(row + col + 1);
-  if (col + 2 < end) v.z = __ldg(row + col + 2);
-  return v;
+// 16-byte asynchronous copy global -> shared (cp.async, cached in L2 only).
+// `bytes` < 16 copies that many bytes and fills the rest of the 16 with
+// zeros; bytes == 0 reads nothing (src is then any valid address).
+__device__ __forceinline__ void cp_async16(void* dst, const float* src, int bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dev::smem_addr(dst)),
+               "l"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Waits until at most `n` of this thread's most recent copy groups are pending.
+template <int n>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory");
 }
 
-// Loads k-slice [k0, k0 + 16) of the tile, clipped to [.., k_end) and to M, N.
-// A: thread i = tid + 128 j holds rows (i mod 64), k quad (i div 64), so a warp
-// touches 32 consecutive rows and the transposed stores are conflict-free.
-// B: thread i holds k row (i div 16), column quad (i mod 16).
-__device__ __forceinline__ void load_slice(const SmallArgs& p, int m0, int n0, int k0, int k_end,
-                                           int tid, Slice& s) {
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int i = tid + kSmThreads * j;
-    const int row = i & 63, kq = i >> 6;
-    const int64_t m = int64_t(m0) + row;
-    s.a[j] = m < p.M ? load4(p.A + m * p.lda, k0 + 4 * kq, k_end) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int i = tid + kSmThreads * j;
-    const int kr = i >> 4, cq = i & 15;
-    const int64_t k = int64_t(k0) + kr;
-    s.b[j] = k < k_end ? load4(p.B + k * p.ldb, int64_t(n0) + 4 * cq, p.N)
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-}
-
-// Shared memory: A k-major ([k][m], transposed on the way in), B as is ([k][n]).
+// Shared memory: a ring of k-slices, A as rows ([m][k], 64 bytes a row) and
+// B as is ([k][n]).
 struct SmallSmem {
-  float a[2][kSmBK][kSmBM];
-  float b[2][kSmBK][kSmBN];
+  float a[kSmStages][kSmBM][kSmBK];
+  float b[kSmStages][kSmBK][kSmBN];
   int last;
 };
 
-__device__ __forceinline__ void store_slice(SmallSmem& sm, int buf, int tid, const Slice& s) {
+// Copies k-slice [k0, k0 + 16) of the tile into ring stage `st`: 16-byte
+// chunks, two of A and two of B per thread, clipped to M, N and k_end (the
+// copies zero-fill what lies outside).  A: thread i = tid + 128 j copies row
+// i / 4, k quad i % 4 (a warp covers 8 whole rows); B: row i / 16, column
+// quad i % 16 (a warp covers two rows of 64 columns).
+__device__ __forceinline__ void issue_slice(const SmallArgs& p, SmallSmem& sm, int st, int m0,
+                                            int n0, int k0, int k_end, int tid) {
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     const int i = tid + kSmThreads * j;
-    const int row = i & 63, kq = i >> 6;
-    sm.a[buf][4 * kq + 0][row] = s.a[j].x;
-    sm.a[buf][4 * kq + 1][row] = s.a[j].y;
-    sm.a[buf][4 * kq + 2][row] = s.a[j].z;
-    sm.a[buf][4 * kq + 3][row] = s.a[j].w;
+    const int row = i >> 2, kq = i & 3;
+    const int64_t m = int64_t(m0) + row;
+    const int k = k0 + 4 * kq;
+    const int bytes = m < p.M ? 4 * max(0, min(4, k_end - k)) : 0;
+    cp_async16(&sm.a[st][row][4 * kq], bytes > 0 ? p.A + m * p.lda + k : p.A, bytes);
   }
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     const int i = tid + kSmThreads * j;
     const int kr = i >> 4, cq = i & 15;
-    *reinterpret_cast<float4*>(&sm.b[buf][kr][4 * cq]) = s.b[j];
+    const int k = k0 + kr;
+    const int64_t n = int64_t(n0) + 4 * cq;
+    const int bytes = k < k_end ? int(4 * max(int64_t(0), min(int64_t(4), p.N - n))) : 0;
+    cp_async16(&sm.b[st][kr][4 * cq], bytes > 0 ? p.B + int64_t(k) * p.ldb + n : p.B, bytes);
   }
 }
 
@@ -106,31 +95,47 @@ __global__ void __launch_bounds__(kSmThreads)
 #pragma unroll
     for (int q = 0; q < 4; ++q) acc[r][q] = make_float2(0.f, 0.f);
 
-  Slice s;
-  if (nk > 0) {
-    load_slice(p, m0, n0, k_begin, k_end, tid, s);
-    store_slice(sm, 0, tid, s);
+  // Ring of kSmStages k-slices: the copies of up to three slices are in
+  // flight while one is computed, so a short K does not pay one global round
+  // trip per slice.  One copy group per slice, committed even when empty so
+  // that the group count stays aligned with the slice index.
+#pragma unroll
+  for (int st = 0; st < kSmStages - 1; ++st) {
+    if (st < nk) issue_slice(p, sm, st, m0, n0, k_begin + st * kSmBK, k_end, tid);
+    cp_async_commit();
   }
-  __syncthreads();
+#pragma unroll 1
   for (int kt = 0; kt < nk; ++kt) {
-    const int buf = kt & 1;
-    if (kt + 1 < nk) load_slice(p, m0, n0, k_begin + (kt + 1) * kSmBK, k_end, tid, s);
+    cp_async_wait<kSmStages - 2>();  // slice kt has landed (this thread's copies)
+    __syncthreads();                 // ... and every thread's; slice kt - 1 is free
+    const int nxt = kt + kSmStages - 1;
+    if (nxt < nk) issue_slice(p, sm, nxt % kSmStages, m0, n0, k_begin + nxt * kSmBK, k_end, tid);
+    cp_async_commit();
+    const int st = kt % kSmStages;
 #pragma unroll
-    for (int kk = 0; kk < kSmBK; ++kk) {
-      const float4 a = *reinterpret_cast<const float4*>(&sm.a[buf][kk][4 * ty]);
-      const float4 b0 = *reinterpret_cast<const float4*>(&sm.b[buf][kk][4 * tx]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&sm.b[buf][kk][32 + 4 * tx]);
-      const float av[4] = {a.x, a.y, a.z, a.w};
-      const float2 bq[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
-                            make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
+    for (int k4 = 0; k4 < kSmBK / 4; ++k4) {
+      // A at rows 4 ty .. 4 ty + 3, k = 4 k4 .. 4 k4 + 3 (one 128-bit load a row).
+      float4 a[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
+      for (int r = 0; r < 4; ++r) a[r] = *reinterpret_cast<const float4*>(&sm.a[st][4 * ty + r][4 * k4]);
 #pragma unroll
-        for (int r = 0; r < 4; ++r) dev::ffma2(acc[r][q], make_float2(av[r], av[r]), bq[q]);
+      for (int kk = 0; kk < 4; ++kk) {
+        const int k = 4 * k4 + kk;
+        const float4 b0 = *reinterpret_cast<const float4*>(&sm.b[st][k][4 * tx]);
+        const float4 b1 = *reinterpret_cast<const float4*>(&sm.b[st][k][32 + 4 * tx]);
+        const float2 bq[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
+                              make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const float av = kk == 0 ? a[r].x : kk == 1 ? a[r].y : kk == 2 ? a[r].z : a[r].w;
+            dev::ffma2(acc[r][q], make_float2(av, av), bq[q]);
+          }
+      }
     }
-    if (kt + 1 < nk) store_slice(sm, buf ^ 1, tid, s);
-    __syncthreads();
   }
+  cp_async_wait<0>();  // no copy is left pending when the CTA moves on
 
   // Output value j (0..7) of this thread: row 4 ty + (j / 2), column quad j % 2.
   auto value = [&](int j) {
