@@ -39,16 +39,18 @@ constexpr double kGuardedTflops = 23.0;     // large products
 constexpr double kGuardedStepUs = 1.6;      // one 16-deep step of a CTA (a global-load round trip)
 constexpr double kGuardedCtasPerSm = 4.0;   // 256 threads x 64 registers
 constexpr double kCopyBytesPerUs = 4.5e6;
-// Small-product kernel: CTAs per SM it is sized for (128 threads x 128
-// registers); the time of one 16-deep slice of a 64 x 64 tile when the SM
-// runs one CTA (latency bound) and when it runs four (arithmetic bound);
-// the fixed cost of a launch; the reduction cost per share of a split tile
-// (the last share reads every other share's 16 KB partial).  Fitted to
-// GB300 timings with forced split counts from 256^3 to 768^3.
+// Small-product kernel: the time of one 16-deep slice of a 64 x 64 tile
+// when the SM runs one CTA (latency bound: the copy ring keeps three slices
+// in flight) and the time per four CTAs an SM runs (arithmetic bound); the
+// fixed cost of a launch; the reduction of a split tile, a fixed part
+// (publishing, the arrival counter) and a part per share (the last share
+// reads every other share's 16 KB partial).  Fitted to GB300 timings with
+// forced split counts from 64^3 to 1024^3 and K up to 4096.
 constexpr int kSmallCtasPerSm = 4;
-constexpr double kSmallSliceUs = 0.75;
-constexpr double kSmallFullSliceUs = 2.3;
-constexpr double kSmallFixedUs = 5.0;
+constexpr double kSmallSliceUs = 0.55;
+constexpr double kSmallFullSliceUs = 1.9;
+constexpr double kSmallFixedUs = 4.6;
+constexpr double kSmallReduceUs = 1.2;
 constexpr double kSmallShareUs = 0.45;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -233,14 +235,15 @@ bool is_fast(int v) {
 
 // Estimated duration (microseconds) of the small-product kernel for `grid`
 // CTAs of `slices` 16-deep slices each, the tiles split into `splits` shares.
+// Each SM works through its CTAs' slices at the arithmetic rate
+// (kSmallFullSliceUs per slice of four CTAs), but no faster than one slice
+// per kSmallSliceUs.
 double small_cost_us(int64_t grid, int64_t slices, int64_t splits, const DeviceState& ds) {
   const double per_sm = std::ceil(double(grid) / double(ds.sms));
-  const double waves = std::ceil(per_sm / kSmallCtasPerSm);
-  const double busy = per_sm < kSmallCtasPerSm ? per_sm : double(kSmallCtasPerSm);
-  double slice_us = kSmallFullSliceUs * busy / kSmallCtasPerSm;
+  double slice_us = kSmallFullSliceUs * per_sm / kSmallCtasPerSm;
   if (slice_us < kSmallSliceUs) slice_us = kSmallSliceUs;
-  const double reduce = splits > 1 ? 0.5 + kSmallShareUs * double(splits) : 0.0;
-  return kSmallFixedUs + waves * double(slices) * slice_us + reduce;
+  const double reduce = splits > 1 ? kSmallReduceUs + kSmallShareUs * double(splits) : 0.0;
+  return kSmallFixedUs + double(slices) * slice_us + reduce;
 }
 
 // The small-product kernel: the number of K shares per tile (a power of two,
