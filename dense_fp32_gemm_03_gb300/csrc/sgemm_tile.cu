@@ -115,9 +115,12 @@ struct TileCfg {
 };
 
 // The compiled tile configurations (index = TileConfig id).
-using Cfg0 = TileCfg<4, 2, 16, 4, 4, false, 1, 56, true>;   // 128 x 256 tile, 8 + 4 warps, 8x16 patch
-using Cfg1 = TileCfg<4, 2, 16, 4, 4, false, 1>;             // Cfg0, one-row quarter-warps
-using Cfg2 = TileCfg<4, 2, 16, 4, 4, true, 1, 56, true>;    // Cfg1 with fragment double buffering
+// The 128 x 256 configurations keep six k-tiles in the ring (176 KB of
+// shared memory): with four, the compute warps waited for data whenever A
+// and B exceed L2 (4096^3: 3 % slower); eight left L1 too small (2.6 %).
+using Cfg0 = TileCfg<4, 2, 16, 6, 4, false, 1, 56, true>;   // 128 x 256 tile, 8 + 4 warps, 8x16 patch
+using Cfg1 = TileCfg<4, 2, 16, 6, 4, false, 1>;             // Cfg0, one-row quarter-warps
+using Cfg2 = TileCfg<4, 2, 16, 6, 4, true, 1, 56, true>;    // Cfg1 with fragment double buffering
 using Cfg3 = TileCfg<4, 2, 8, 4, 4, true, 1>;               // 128 x 128 tile, 8 + 4 warps, 8x8 patch
 using Cfg4 = TileCfg<4, 2, 8, 4, 4, true, 1, 56, true>;     // Cfg3, paired-column lane layout
 using Cfg5 = TileCfg<4, 2, 8, 4, 4, false, 1, 56, true>;    // Cfg4 without double buffering
