@@ -436,10 +436,6 @@ sgemm_status_t get_workspace_bytes(int dev, cudaStream_t stream, size_t need, vo
   return SGEMM_OK;
 }
 
-sgemm_status_t get_workspace(int dev, cudaStream_t stream, const Plan& p, void** out) {
-  return get_workspace_bytes(dev, stream, p.workspace_bytes(), out);
-}
-
 // Tensor maps of the pipelined kernel: A (K fastest) in boxes of 16 x
 // a_box_rows with the 64-byte swizzle, B (N fastest) in boxes of BN x 16.
 sgemm_status_t encode_operands(const TileShape& ts, int64_t M, int64_t N, int64_t K, const float* A,
