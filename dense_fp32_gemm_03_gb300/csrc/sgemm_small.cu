@@ -41,7 +41,12 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 // Shared memory: a ring of k-slices, A as rows ([m][k], 64 bytes a row) and
-// B as is ([k][n]).
+// B as is ([k][n]).  The four 16-byte k-chunks of an A row are stored in the
+// order kq ^ ((row / 4) % 4): a warp reads one chunk from each of four rows
+// 256 bytes apart, which would otherwise fall on the same four banks; with
+// the swizzle the four chunks cover sixteen different banks.
+__device__ __forceinline__ int a_chunk(int row, int kq) { return kq ^ ((row >> 2) & 3); }
+
 struct SmallSmem {
   float a[kSmStages][kSmBM][kSmBK];
   float b[kSmStages][kSmBK][kSmBN];
@@ -62,7 +67,7 @@ __device__ __forceinline__ void issue_slice(const SmallArgs& p, SmallSmem& sm, i
     const int64_t m = int64_t(m0) + row;
     const int k = k0 + 4 * kq;
     const int bytes = m < p.M ? 4 * max(0, min(4, k_end - k)) : 0;
-    cp_async16(&sm.a[st][row][4 * kq], bytes > 0 ? p.A + m * p.lda + k : p.A, bytes);
+    cp_async16(&sm.a[st][row][4 * a_chunk(row, kq)], bytes > 0 ? p.A + m * p.lda + k : p.A, bytes);
   }
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
@@ -117,7 +122,8 @@ __global__ void __launch_bounds__(kSmThreads)
       // A at rows 4 ty .. 4 ty + 3, k = 4 k4 .. 4 k4 + 3 (one 128-bit load a row).
       float4 a[4];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) a[r] = *reinterpret_cast<const float4*>(&sm.a[st][4 * ty + r][4 * k4]);
+      for (int r = 0; r < 4; ++r)
+        a[r] = *reinterpret_cast<const float4*>(&sm.a[st][4 * ty + r][4 * a_chunk(4 * ty + r, k4)]);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const int k = 4 * k4 + kk;
