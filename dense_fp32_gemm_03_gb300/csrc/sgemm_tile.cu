@@ -2,7 +2,7 @@
 //
 // C = A * B, row-major FP32, alpha = 1, beta = 0 ("Beyond Kernel 7: Closing
 // the Gap to cuBLAS on an H100 FP32 GEMM", section "The operation").  One
-// kernel template serves three schedules (Sched in sgemm_internal.h): one
+// kernel template serves three schedules (Sched in sgemm_plan.h): one
 // tile per CTA, persistent whole-tile waves, and Stream-K splits of K.
 //
 // Roles inside a CTA:
