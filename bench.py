@@ -56,6 +56,8 @@ def parse_args(argv=None):
                    help="target host time of the oracle sample")
     p.add_argument("--sweep", action="store_true",
                    help="one JSON line per workload of the configuration list (not the default line)")
+    p.add_argument("--sweep-cpu-seconds", type=float, default=2.0,
+                   help="host time of each oracle sample in --sweep (0: no oracle timing)")
     return p.parse_args(argv)
 
 
@@ -209,9 +211,20 @@ def measured_traffic(workload: str):
     return float(traffic.group(1))
 
 
-def cpu_baseline(w, A, B, seconds: float):
-    """Time the oracle (as it stands) on a bounded row sample of the workload."""
+def cpu_baseline(w, A, B, seconds: float, threads: int = 0):
+    """Time the oracle (as it stands) on a bounded row sample of the workload, on all
+    the host cores it may use (threads <= 0) or on `threads` of them."""
     import oracle
+    all_cores = oracle.max_threads()
+    if threads > 0:
+        oracle.set_threads(threads)
+    try:
+        return _cpu_sample(w, A, B, seconds, oracle)
+    finally:
+        oracle.set_threads(all_cores)
+
+
+def _cpu_sample(w, A, B, seconds, oracle):
     cores = oracle.max_threads()
     rows = max(1, min(w.M, cores))
     t0 = time.perf_counter()
@@ -219,14 +232,19 @@ def cpu_baseline(w, A, B, seconds: float):
     dt = time.perf_counter() - t0
     rows2 = int(min(w.M, max(rows, rows * seconds / max(dt, 1e-6))))
     rows2 = max(rows, (rows2 // cores) * cores) if rows2 >= cores else rows2
+    # A product small enough to finish well inside the budget is repeated.
+    reps = max(1, int(seconds / max(dt * rows2 / rows, 1e-6))) if rows2 == w.M else 1
     t0 = time.perf_counter()
-    oracle.sgemm_f64(A[:rows2], B, with_abs=False)
-    dt2 = time.perf_counter() - t0
+    for _ in range(reps):
+        oracle.sgemm_f64(A[:rows2], B, with_abs=False)
+    total = time.perf_counter() - t0
+    dt2 = total / reps
     flops = 2.0 * rows2 * w.N * w.K
+    rep_note = f", {reps} repetitions" if reps > 1 else ""
     return {"value": flops / dt2 / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"rows 0..{rows2 - 1} of the {w.M}x{w.N}x{w.K} product ({rows2}x{w.N} outputs, "
-                      f"float64 triple loop, {dt2:.1f} s)",
-            "seconds": dt2}
+                      f"float64 triple loop{rep_note}, {total:.1f} s)",
+            "seconds": total}
 
 
 # ------------------------------------------------------------------------- arms
@@ -441,13 +459,22 @@ def run_ours(args):
         for w in workloads.ALL:
             if w.dist == "int8range":
                 continue
-            *_, times, chosen = bench_workload(w, args, sg, device, flush, variant)
+            A_h, B_h, *_, times, chosen = bench_workload(w, args, sg, device, flush, variant)
             ms = statistics.median(times)
-            print(json.dumps({"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
-                              "variant": sg.variant_name(chosen), "us_median": ms * 1e3,
-                              "us_p10": sorted(times)[len(times) // 10] * 1e3,
-                              "us_p90": sorted(times)[(9 * len(times)) // 10] * 1e3,
-                              "tflops": w.flops / (ms * 1e-3) / 1e12}), flush=True)
+            line = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+                    "variant": sg.variant_name(chosen), "us_median": ms * 1e3,
+                    "us_p10": sorted(times)[len(times) // 10] * 1e3,
+                    "us_p90": sorted(times)[(9 * len(times)) // 10] * 1e3,
+                    "tflops": w.flops / (ms * 1e-3) / 1e12}
+            if args.sweep_cpu_seconds > 0 and rank == 0:
+                # The oracle on the host cores, a reported baseline only: all cores for
+                # every workload, one core as well up to 1024^3.
+                cpu = {"all_cores": cpu_baseline(w, A_h, B_h, args.sweep_cpu_seconds)}
+                if max(w.M, w.N, w.K) <= 1024:
+                    cpu["one_core"] = cpu_baseline(w, A_h, B_h, args.sweep_cpu_seconds, threads=1)
+                line["cpu_oracle"] = {k: {"tflops": v["value"], "cores": v["cores"], "sample": v["sample"]}
+                                      for k, v in cpu.items()}
+            print(json.dumps(line), flush=True)
         return 0
 
     w = workloads.BY_NAME[args.workload]
