@@ -1,0 +1,24 @@
+// Host probe of the tile kernel's work decomposition, for tests/test_plan_host.py.
+//
+// Reads lines "M N K BM BN BK resident streamk" from stdin and prints, per
+// line, the plan_launch() result: "ok tiles_m tiles_n iters_per_tile dp_tiles
+// sk_tiles sk_ctas sk_base sk_extra grid slots group_m".  plan_launch is the
+// constexpr function that the host API and the size-specialized kernels both
+// evaluate, so this is the decomposition the GPU runs.
+#include <cstdio>
+
+#include "sgemm_plan.h"
+
+int main() {
+  long long M, N, K, resident;
+  int bm, bn, bk, streamk;
+  while (std::scanf("%lld %lld %lld %d %d %d %lld %d", &M, &N, &K, &bm, &bn, &bk, &resident,
+                    &streamk) == 8) {
+    const gb300::LaunchPlan p = gb300::plan_launch(M, N, K, bm, bn, bk, resident, streamk != 0);
+    std::printf("%d %d %d %d %d %d %d %d %d %lld %lld %d\n", p.ok ? 1 : 0, p.sc.tiles_m,
+                p.sc.tiles_n, p.sc.iters_per_tile, p.sc.dp_tiles, p.sc.sk_tiles, p.sc.sk_ctas,
+                p.sc.sk_base, p.sc.sk_extra, static_cast<long long>(p.grid),
+                static_cast<long long>(p.slots), p.sc.group_m);
+  }
+  return 0;
+}
