@@ -22,8 +22,11 @@
  * per (device, stream): the first call that needs more than the cache holds
  * allocates it with cudaMalloc (so make that first call outside stream
  * capture); later calls reuse it.  Calls on one stream are ordered; calls on
- * different streams use different workspaces.  sgemm_release_workspaces()
- * frees the cache.
+ * different streams use different workspaces.  Calls on one stream must not
+ * be made from several host threads at the same time: one call may regrow the
+ * stream's workspace while another is still enqueuing work that uses it.
+ * Threads on different streams are safe.  sgemm_release_workspaces() frees
+ * the cache.
  *
  * Errors.  Every entry point returns an sgemm_status_t and never aborts the
  * process.  Argument errors are found on the host before any launch.  A
