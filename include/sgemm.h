@@ -74,7 +74,7 @@ typedef enum {
  * M == 0 or N == 0: nothing to do, SGEMM_OK.  K == 0: C is filled with zeros
  * (the empty sum).  Any stride and alignment is accepted.  The pipelined
  * kernels read A and B by TMA, and the small-product kernel (SMALL, chosen
- * for products up to roughly 512^3 and for thin or deep shapes whose tiles
+ * for products up to roughly 640^3 and for thin or deep shapes whose tiles
  * would leave SMs idle) with 128-bit loads: both need 16-byte-aligned base
  * addresses and row strides that are multiples of 4 floats.  An operand
  * without that property (for instance a contiguous matrix with an odd number
