@@ -122,7 +122,7 @@ sgemm_status_t sgemm_ex(int layout, int64_t M, int64_t N, int64_t K, float alpha
  * SPECIALIZED is the size-specialized form of the pipelined kernel ("Beyond
  * Kernel 7", the size-specialized kernel of the confirmed 4096 result): the
  * instance with M, N, K and the Stream-K schedule compiled in as constants,
- * built for M = N = K = 1024 and M = N = K = 4096 on a 152-SM GB300.  It
+ * built for M = N = K = 768, 1024, 1536, 2048 and 4096 on a 152-SM GB300.  It
  * computes exactly what the generic Stream-K variant of the same schedule
  * computes (bit for bit).  The selector takes it whenever the shape, the
  * device and aligned operands allow.  Forced with operands the pipelined
