@@ -172,13 +172,14 @@ def sgemm_ex(A, B, C, alpha=1.0, beta=0.0, layout=ROW_MAJOR, stream=None):
         if t.shape[0] > 1 and t.stride(0) != 1:
             raise ValueError(f"{name} must have unit row stride")
         return max(t.stride(1), t.shape[0], 1)
+    lda, ldb, ldc = ld(A, "A"), ld(B, "B"), ld(C, "C")
     M, K = A.shape
     K2, N = B.shape
     if K != K2 or tuple(C.shape) != (M, N):
         raise ValueError(f"shapes do not match: {tuple(A.shape)} @ {tuple(B.shape)} -> {tuple(C.shape)}")
     with torch.cuda.device(A.device):
-        st = load().sgemm_ex(int(layout), M, N, K, float(alpha), A.data_ptr(), ld(A, "A"),
-                             B.data_ptr(), ld(B, "B"), float(beta), C.data_ptr(), ld(C, "C"),
+        st = load().sgemm_ex(int(layout), M, N, K, float(alpha), A.data_ptr(), lda,
+                             B.data_ptr(), ldb, float(beta), C.data_ptr(), ldc,
                              _stream_handle(A.device, stream))
     if st != OK:
         raise SgemmError(st, "sgemm_ex")

@@ -64,3 +64,15 @@ def test_profile_traffic_applies_to_its_kernel_source_only(monkeypatch):
     monkeypatch.setattr(bench, "kernel_source_digest", lambda: "0" * 64)
     assert bench.measured_traffic("square_4096_uniform") is None
     assert bench.measured_traffic("no_such_workload") is None
+
+
+def test_host_tensors_are_refused():
+    """The tensor API computes on the GPU only: host tensors raise, nothing is computed."""
+    import pytest
+    import torch
+    import dense_fp32_gemm_03_gb300 as sg
+    A = torch.ones(4, 4)
+    for call in (lambda: sg.sgemm(A, A), lambda: sg.sgemm_tf32(A, A),
+                 lambda: sg.sgemm_ex(A, A, torch.zeros(4, 4))):
+        with pytest.raises(ValueError, match="CUDA tensor"):
+            call()
