@@ -15,7 +15,11 @@ C triple loop in ``ref_sgemm.c`` that widens every FP32 input to float64
 Pins (``tests/test_oracle_pins.py``): identity and permutation matrices,
 the rank-1 closed form, brute force against exact rational arithmetic on all
 shapes 1..8, an independent float64 library product, K-split additivity and
-the transpose identity.
+the transpose identity.  The scaled forms: ``sgemm_ex_f64`` (alpha, beta,
+row- or column-major storage) and ``sgemm_op_f64`` (the same with a
+transposition flag per operand, op(A) = A or A^T, op(B) = B or B^T), pinned
+by integer products of explicit transposes, bit-identity with the plain
+definition on explicitly transposed operands, and the transpose identity.
 """
 from __future__ import annotations
 
@@ -62,6 +66,10 @@ def _load():
             lib.ref_sgemm_ex_f64.argtypes = [ctypes.c_int, i64, i64, i64, ctypes.c_double, fp, i64, fp,
                                              i64, ctypes.c_double, fp, i64, dp, i64]
             lib.ref_sgemm_ex_f64.restype = ctypes.c_int
+            lib.ref_sgemm_op_f64.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, i64, i64,
+                                             ctypes.c_double, fp, i64, fp, i64, ctypes.c_double, fp,
+                                             i64, dp, i64]
+            lib.ref_sgemm_op_f64.restype = ctypes.c_int
             lib.ref_set_threads.argtypes = [ctypes.c_int]
             lib.ref_set_threads.restype = None
             lib.ref_max_threads.argtypes = []
@@ -174,6 +182,49 @@ def sgemm_ex_f64(A, B, alpha=1.0, beta=0.0, C0=None, col_major=False):
                                   out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), max(N, 1))
     if st != 0:
         raise ValueError(f"ref_sgemm_ex_f64 rejected its arguments (status {st})")
+    return out
+
+
+def sgemm_op_f64(A, B, trans_a=False, trans_b=False, alpha=1.0, beta=0.0, C0=None,
+                 col_major=False):
+    """alpha * (op(A) . op(B)) + beta * C0 in float64 (M x N, row-major result).
+
+    ``A`` and ``B`` are the STORED float32 arrays: A is M x K, or K x M when
+    ``trans_a`` (op(A) = A^T); B is K x N, or N x K when ``trans_b``.  With
+    ``col_major`` they (and C0) are taken in Fortran order, as for
+    ``sgemm_ex_f64``.  beta == 0 never reads C0.
+    """
+    def prep(x, name):
+        if hasattr(x, "detach"):
+            x = x.detach().numpy()
+        x = np.asarray(x)
+        if x.dtype != np.float32 or x.ndim != 2:
+            raise ValueError(f"{name}: expected a 2-D float32 array")
+        if col_major:
+            x = np.asfortranarray(x)
+            return x, max(x.shape[0], 1)
+        x = np.ascontiguousarray(x)
+        return x, max(x.shape[1], 1)
+    A, lda = prep(A, "A")
+    B, ldb = prep(B, "B")
+    M, K = (A.shape[1], A.shape[0]) if trans_a else A.shape
+    K2, N = (B.shape[1], B.shape[0]) if trans_b else B.shape
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: op(A) {M}x{K}, op(B) {K2}x{N}")
+    if beta != 0.0:
+        C0, ldc = prep(C0, "C0")
+        if C0.shape != (M, N):
+            raise ValueError("C0 has the wrong shape")
+        c0p = _fptr(C0)
+    else:
+        ldc, c0p = max(M if col_major else N, 1), None
+    out = np.zeros((M, N), dtype=np.float64)
+    st = _load().ref_sgemm_op_f64(int(bool(col_major)), int(bool(trans_a)), int(bool(trans_b)),
+                                  M, N, K, float(alpha), _fptr(A), lda, _fptr(B), ldb, float(beta),
+                                  c0p, ldc, out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                                  max(N, 1))
+    if st != 0:
+        raise ValueError(f"ref_sgemm_op_f64 rejected its arguments (status {st})")
     return out
 
 

@@ -139,6 +139,47 @@ int ref_sgemm_ex_f64(int col_major, int64_t M, int64_t N, int64_t K, double alph
   return REF_OK;
 }
 
+/* Element (r, c) of a matrix stored with leading dimension ld. */
+static float ref_at(const float *X, int64_t ld, int col_major, int64_t r, int64_t c) {
+  return col_major ? X[r + c * ld] : X[r * ld + c];
+}
+
+/*
+ * The general form with a transposition flag per operand, the BLAS-style
+ * op() the same epilogue is usually paired with:
+ *   C[m, n] = alpha * (sum_k op(A)[m, k] op(B)[k, n]) + beta * C0[m, n],
+ * op(A) = A (stored M x K) when trans_a == 0 and A^T (A stored K x M, so
+ * op(A)[m, k] is the stored element (k, m)) otherwise; likewise op(B) = B
+ * (stored K x N) or B^T (stored N x K).  Storage order (row- or column-major)
+ * is `col_major`, as in ref_sgemm_ex_f64, and applies to A, B and C0; Cout is
+ * row-major double.  The sum runs over k = 0, 1, ..., K-1 in double, every
+ * product exact.  beta == 0 never reads C0.
+ */
+int ref_sgemm_op_f64(int col_major, int trans_a, int trans_b, int64_t M, int64_t N, int64_t K,
+                     double alpha, const float *A, int64_t lda, const float *B, int64_t ldb,
+                     double beta, const float *C0, int64_t ldc, double *Cout, int64_t ldo) {
+  if (M < 0 || N < 0 || K < 0) return REF_INVALID;
+  if (M == 0 || N == 0) return REF_OK;
+  if (Cout == NULL || ldo < N) return REF_INVALID;
+  if (beta != 0.0 && C0 == NULL) return REF_INVALID;
+  if (K > 0 && (A == NULL || B == NULL)) return REF_INVALID;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t m = 0; m < M; ++m) {
+    for (int64_t n = 0; n < N; ++n) {
+      double s = 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        const float a = trans_a ? ref_at(A, lda, col_major, k, m) : ref_at(A, lda, col_major, m, k);
+        const float b = trans_b ? ref_at(B, ldb, col_major, n, k) : ref_at(B, ldb, col_major, k, n);
+        s += (double)a * (double)b;
+      }
+      double r = alpha * s;
+      if (beta != 0.0) r += beta * (double)ref_at(C0, ldc, col_major, m, n);
+      Cout[m * ldo + n] = r;
+    }
+  }
+  return REF_OK;
+}
+
 /* Thread control for timing: 0 or less leaves the OpenMP default. */
 void ref_set_threads(int n) {
 #ifdef _OPENMP

@@ -302,3 +302,148 @@ def test_ex_column_major_is_the_same_product():
     col = oracle.sgemm_ex_f64(np.asfortranarray(A), np.asfortranarray(B), alpha=0.5, beta=2.0,
                               C0=np.asfortranarray(C0), col_major=True)
     assert np.array_equal(row, col)
+
+
+# ------------------------------- per-operand transposition: the op() form
+# op(A) = A or A^T and op(B) = B or B^T, the stored arrays being A (M x K or
+# K x M) and B (K x N or N x K).  Pins, each a function of an ``op`` callable
+# (stored A, stored B, trans_a, trans_b, col_major, alpha, beta, C0) so that
+# planted mistakes can be shown to fail one:
+# * small integers: exact against numpy int64 products of explicit transposes,
+#   with alpha, beta and both storage orders, on square and non-square shapes;
+# * random floats: bit-identical to the plain pinned oracle applied to the
+#   explicitly transposed (contiguous) operands -- the same products summed
+#   in the same k order;
+# * the transpose identity (op(A) op(B))^T = op(B)^T op(A)^T, bit-exact.
+TRANS = [(False, False), (True, False), (False, True), (True, True)]
+
+
+def _op_oracle(A, B, ta, tb, col_major=False, alpha=1.0, beta=0.0, C0=None):
+    return oracle.sgemm_op_f64(A, B, trans_a=ta, trans_b=tb, alpha=alpha, beta=beta, C0=C0,
+                               col_major=col_major)
+
+
+def _stored(x, t):
+    return np.ascontiguousarray(x.T if t else x).astype(np.float32)
+
+
+def pin_op_integer_exact(op):
+    rng = _rng(21)
+    for M, N, K in [(7, 5, 9), (6, 6, 6)]:
+        for ta, tb in TRANS:
+            for cm in (False, True):
+                opA = rng.integers(-8, 9, size=(M, K)).astype(np.int64)
+                opB = rng.integers(-8, 9, size=(K, N)).astype(np.int64)
+                C0 = rng.integers(-8, 9, size=(M, N)).astype(np.int64)
+                expect = (3 * (opA @ opB) - 2 * C0).astype(np.float64)
+                got = op(_stored(opA, ta), _stored(opB, tb), ta, tb, cm, alpha=3.0, beta=-2.0,
+                         C0=C0.astype(np.float32))
+                assert np.array_equal(got, expect), (M, N, K, ta, tb, cm)
+
+
+def pin_op_explicit_transposes(op):
+    rng = _rng(22)
+    for M, N, K in [(9, 4, 13), (8, 8, 8)]:
+        opA = rng.standard_normal((M, K)).astype(np.float32)
+        opB = rng.standard_normal((K, N)).astype(np.float32)
+        plain = oracle.sgemm_f64(opA, opB, with_abs=False)[0]
+        for ta, tb in TRANS:
+            got = op(_stored(opA, ta), _stored(opB, tb), ta, tb)
+            assert np.array_equal(got, plain), (M, N, K, ta, tb)
+
+
+def pin_op_transpose_identity(op):
+    rng = _rng(23)
+    for M, N, K in [(5, 11, 7), (6, 6, 6)]:
+        opA = rng.standard_normal((M, K)).astype(np.float32)
+        opB = rng.standard_normal((K, N)).astype(np.float32)
+        for ta, tb in TRANS:
+            A, B = _stored(opA, ta), _stored(opB, tb)
+            C = op(A, B, ta, tb)
+            # op(B)^T is the stored B read with the other flag; likewise op(A)^T.
+            Ct = op(B, A, not tb, not ta)
+            assert np.array_equal(C.T, Ct), (M, N, K, ta, tb)
+
+
+OP_PINS = [pin_op_integer_exact, pin_op_explicit_transposes, pin_op_transpose_identity]
+
+
+@pytest.mark.parametrize("pin", OP_PINS, ids=lambda p: p.__name__)
+def test_op_oracle_pin(pin):
+    pin(_op_oracle)
+
+
+def _op_reference_parts(A, B, ta, tb):
+    opA = (A.T if ta else A).astype(np.float64)
+    opB = (B.T if tb else B).astype(np.float64)
+    return opA, opB
+
+
+def _opmut_swapped_flags(A, B, ta, tb, col_major=False, alpha=1.0, beta=0.0, C0=None):
+    """Applies trans_b to A and trans_a to B."""
+    opA, opB = _op_reference_parts(A, B, tb, ta)
+    r = alpha * (opA @ opB)
+    return r + beta * C0.astype(np.float64) if beta != 0 else r
+
+
+def _opmut_ignores_trans_a(A, B, ta, tb, col_major=False, alpha=1.0, beta=0.0, C0=None):
+    opA, opB = _op_reference_parts(A, B, False, tb)
+    r = alpha * (opA @ opB)
+    return r + beta * C0.astype(np.float64) if beta != 0 else r
+
+
+def _opmut_c0_transposed(A, B, ta, tb, col_major=False, alpha=1.0, beta=0.0, C0=None):
+    """Reads C0 transposed whenever A is transposed."""
+    opA, opB = _op_reference_parts(A, B, ta, tb)
+    r = alpha * (opA @ opB)
+    if beta != 0:
+        c = C0.astype(np.float64)
+        r = r + beta * (c.T if ta else c)
+    return r
+
+
+def _opmut_beta_sign(A, B, ta, tb, col_major=False, alpha=1.0, beta=0.0, C0=None):
+    opA, opB = _op_reference_parts(A, B, ta, tb)
+    r = alpha * (opA @ opB)
+    return r - beta * C0.astype(np.float64) if beta != 0 else r
+
+
+def _opmut_drops_alpha_when_transposed(A, B, ta, tb, col_major=False, alpha=1.0, beta=0.0, C0=None):
+    opA, opB = _op_reference_parts(A, B, ta, tb)
+    r = (1.0 if (ta or tb) else alpha) * (opA @ opB)
+    return r + beta * C0.astype(np.float64) if beta != 0 else r
+
+
+OP_MUTANTS = [_opmut_swapped_flags, _opmut_ignores_trans_a, _opmut_c0_transposed, _opmut_beta_sign,
+              _opmut_drops_alpha_when_transposed]
+
+
+@pytest.mark.parametrize("mutant", OP_MUTANTS, ids=lambda f: f.__name__)
+def test_op_pins_catch_mutants(mutant):
+    failed = 0
+    for pin in OP_PINS:
+        try:
+            pin(mutant)
+        except (AssertionError, ValueError, IndexError):
+            failed += 1
+    assert failed >= 1, f"no pin caught {mutant.__name__}"
+
+
+def test_op_without_transposition_is_the_ex_form():
+    rng = _rng(24)
+    A = rng.standard_normal((10, 7)).astype(np.float32)
+    B = rng.standard_normal((7, 12)).astype(np.float32)
+    C0 = rng.standard_normal((10, 12)).astype(np.float32)
+    for cm in (False, True):
+        assert np.array_equal(
+            oracle.sgemm_op_f64(A, B, alpha=0.75, beta=-1.5, C0=C0, col_major=cm),
+            oracle.sgemm_ex_f64(A, B, alpha=0.75, beta=-1.5, C0=C0, col_major=cm))
+
+
+def test_op_beta_zero_never_reads_c():
+    rng = _rng(25)
+    A = rng.integers(-4, 5, size=(6, 9)).astype(np.float32)
+    B = rng.integers(-4, 5, size=(5, 6)).astype(np.float32)   # stored N x K: trans_b
+    nan_c = np.full((9, 5), np.nan, dtype=np.float32)
+    got = oracle.sgemm_op_f64(A, B, trans_a=True, trans_b=True, beta=0.0, C0=nan_c)
+    assert np.array_equal(got, (A.T.astype(np.int64) @ B.T.astype(np.int64)).astype(np.float64))
