@@ -12,6 +12,7 @@
 #include <map>
 #include <mutex>
 #include <utility>
+#include <vector>
 
 #include "sgemm.h"
 #include "sgemm_internal.h"
@@ -22,8 +23,9 @@ using gb300::Sched;
 using gb300::TileConfig;
 using gb300::TileShape;
 
-// [0] = first sgemm_status_t recorded by a kernel since the last query, [1] = wait site.
-__device__ uint32_t g_status_word[2];
+// [0] = first sgemm_status_t recorded by a kernel since the last query, [1] = wait site;
+// [2..3] = the snapshot a query takes of [0..1] (status_take_kernel).
+__device__ uint32_t g_status_word[4];
 
 constexpr int64_t kInt32Max = 0x7fffffffLL;
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
@@ -70,6 +72,10 @@ struct DeviceState {
 struct Workspace {
   void* ptr = nullptr;
   size_t bytes = 0;
+  // A kernel gave up part-way (timeout) since this workspace was last used:
+  // its arrival counters may be nonzero.  They are cleared on the owning
+  // stream, in stream order, before the next call that uses the workspace.
+  bool dirty = false;
 };
 
 // Compiled tile configuration behind each tile size of the variants; the
@@ -89,6 +95,10 @@ int env_config(const char* name, int fallback) {
 std::mutex g_mu;
 std::map<int, DeviceState> g_devices;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;
+// Workspaces replaced by a larger one.  They stay allocated until
+// sgemm_release_workspaces(): kernels still running, or a CUDA graph captured
+// while one was current, may use them.
+std::vector<std::pair<int, void*>> g_retired;
 EncodeTiledFn g_encode = nullptr;
 
 // Initialises (once) and returns the state of the current device.
@@ -415,13 +425,17 @@ sgemm_status_t get_workspace_bytes(int dev, cudaStream_t stream, size_t need, vo
   Workspace& ws = g_workspaces[{dev, stream}];
   if (ws.bytes < need) {
     if (ws.ptr) {
-      cudaFree(ws.ptr);  // cudaFree waits for the device, so no kernel still uses it
+      // Not freed here: earlier kernels on this stream, or a graph captured
+      // with it, may still use the old buffer (and cudaFree would also wait
+      // for the whole device).
+      g_retired.emplace_back(dev, ws.ptr);
       ws.ptr = nullptr;
       ws.bytes = 0;
     }
     size_t bytes = need + need / 4;
     if (cudaMalloc(&ws.ptr, bytes) != cudaSuccess) {
       cudaGetLastError();
+      ws.ptr = nullptr;
       return SGEMM_ERR_ALLOC;
     }
     // Arrival counters start at zero; every finished tile resets its own.
@@ -431,6 +445,12 @@ sgemm_status_t get_workspace_bytes(int dev, cudaStream_t stream, size_t need, vo
       return SGEMM_ERR_LAUNCH;
     }
     ws.bytes = bytes;
+    ws.dirty = false;
+  } else if (ws.dirty) {
+    // After a timeout: clear the counters behind everything already queued
+    // on this stream, ahead of this call's kernels.
+    if (cudaMemsetAsync(ws.ptr, 0, kCounterBytes, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    ws.dirty = false;
   }
   *out = ws.ptr;
   return SGEMM_OK;
@@ -760,18 +780,24 @@ sgemm_status_t sgemm_query_device_status(cudaStream_t stream, uint32_t* detail) 
   sgemm_status_t st = device_state(&ds, &dev);
   if (detail) *detail = 0;
   if (st != SGEMM_OK) return st;
+  // Take and clear the word on `stream` (an atomic exchange on the device, so
+  // kernels still running on other streams lose no record), then read it.
   uint32_t word[2] = {0, 0};
-  if (cudaStreamSynchronize(stream) != cudaSuccess ||
-      cudaMemcpy(word, ds->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess ||
-      cudaMemset(ds->status, 0, sizeof(word)) != cudaSuccess)
+  if (gb300::launch_status_take(ds->status, stream) != cudaSuccess ||
+      cudaMemcpyAsync(word, ds->status + 2, sizeof(word), cudaMemcpyDeviceToHost, stream) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
     return SGEMM_ERR_LAUNCH;
-  if (detail) *detail = word[1];
   if (word[0] == SGEMM_OK) return SGEMM_OK;
-  // A kernel gave up part-way: its arrival counters may be left nonzero.
+  if (detail) *detail = word[1];
+  // A kernel gave up part-way: its arrival counters may be left nonzero.  The
+  // workspaces of this device are cleared lazily, each on its own stream just
+  // before its next use, so that no kernel still running on another stream
+  // sees its counters change under it.
   {
     std::lock_guard<std::mutex> lock(g_mu);
     for (auto& kv : g_workspaces)
-      if (kv.first.first == dev && kv.second.ptr) cudaMemset(kv.second.ptr, 0, kv.second.bytes);
+      if (kv.first.first == dev && kv.second.ptr) kv.second.dirty = true;
   }
   return sgemm_status_t(word[0]);
 }
@@ -780,14 +806,16 @@ void sgemm_release_workspaces(void) {
   std::lock_guard<std::mutex> lock(g_mu);
   int cur = 0;
   cudaGetDevice(&cur);
-  for (auto& kv : g_workspaces) {
-    if (kv.second.ptr) {
-      cudaSetDevice(kv.first.first);
-      cudaDeviceSynchronize();
-      cudaFree(kv.second.ptr);
-    }
-  }
+  auto release = [](int dev, void* ptr) {
+    cudaSetDevice(dev);
+    cudaDeviceSynchronize();
+    cudaFree(ptr);
+  };
+  for (auto& kv : g_workspaces)
+    if (kv.second.ptr) release(kv.first.first, kv.second.ptr);
+  for (auto& r : g_retired) release(r.first, r.second);
   g_workspaces.clear();
+  g_retired.clear();
   cudaSetDevice(cur);
 }
 
@@ -834,10 +862,10 @@ sgemm_status_t sgemm_debug_expire_wait(uint64_t limit_ns, cudaStream_t stream) {
 // The Stream-K schedule needs scratch memory (arrival counters and the
 // partial sums of split tiles).  sgemm() takes it from a cache that calls
 // cudaMalloc the first time a stream needs more.  Some callers cannot let a
-// library allocate: code that runs while its stream is being captured, code
-// that must never wait on the whole device (cudaMalloc and cudaFree may
-// synchronise it), and code that hands out a fixed memory budget before any
-// work starts.  sgemm_streamk_static() serves them from a fixed array in the
+// library allocate: code that must never wait on the whole device
+// (cudaMalloc and cudaFree may synchronise it), code that hands out a fixed
+// memory budget before any work starts, and code inside a framework whose own
+// allocator owns the device memory.  sgemm_streamk_static() serves them from a fixed array in the
 // library's device image instead.
 namespace {
 

@@ -135,6 +135,15 @@ __global__ void scale_kernel(int64_t M, int64_t N, float* __restrict__ C, int64_
 
 // One CTA waits on a barrier that nothing completes; the bounded wait gives up
 // after limit_ns and the timeout is recorded.  Nothing is in flight.
+// Moves the live status word (status[0..1]) into the snapshot (status[2..3])
+// and clears it, atomically with respect to kernels still recording on other
+// streams: an error recorded after the exchange stays for the next query.
+__global__ void status_take_kernel(uint32_t* status) {
+  const uint32_t code = atomicExch(status, 0u);
+  status[2] = code;
+  status[3] = code != 0u ? atomicExch(status + 1, 0u) : 0u;
+}
+
 __global__ void expire_probe_kernel(uint32_t* status, uint64_t limit_ns) {
   __shared__ __align__(8) uint64_t bar;
   if (threadIdx.x == 0) {
@@ -196,6 +205,11 @@ cudaError_t launch_scale(int64_t M, int64_t N, float* C, int64_t ldc, float beta
 
 cudaError_t launch_expire_probe(uint32_t* status, uint64_t limit_ns, cudaStream_t stream) {
   expire_probe_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_status_take(uint32_t* status, cudaStream_t stream) {
+  status_take_kernel<<<1, 1, 0, stream>>>(status);
   return cudaGetLastError();
 }
 

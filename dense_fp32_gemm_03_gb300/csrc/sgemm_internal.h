@@ -102,4 +102,7 @@ cudaError_t launch_scale(int64_t M, int64_t N, float* C, int64_t ldc, float beta
 
 cudaError_t launch_expire_probe(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
 
+// status[2..3] = status[0..1], then status[0..1] = 0 (status has four words).
+cudaError_t launch_status_take(uint32_t* status, cudaStream_t stream);
+
 }  // namespace gb300

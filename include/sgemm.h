@@ -21,12 +21,20 @@
  * workspace.  sgemm()/sgemm_variant() take it from a cache the library keeps
  * per (device, stream): the first call that needs more than the cache holds
  * allocates it with cudaMalloc (so make that first call outside stream
- * capture); later calls reuse it.  Calls on one stream are ordered; calls on
+ * capture); later calls reuse it.  A workspace replaced by a larger one is not
+ * freed but kept until sgemm_release_workspaces(), so kernels still running
+ * and CUDA graphs captured while it was current keep valid memory; a graph
+ * captured with these calls must not be replayed after
+ * sgemm_release_workspaces().  Calls on one stream are ordered; calls on
  * different streams use different workspaces.  Calls on one stream must not
- * be made from several host threads at the same time: one call may regrow the
- * stream's workspace while another is still enqueuing work that uses it.
- * Threads on different streams are safe.  sgemm_release_workspaces() frees
- * the cache.
+ * be made from several host threads at the same time: the staged variant
+ * copies operands into the workspace in a launch of its own, and another
+ * thread's call enqueued in between would overwrite them.  Threads on
+ * different streams are safe.  sgemm_release_workspaces() frees the cache.
+ * Independently of that cache, the library's device image holds a fixed
+ * 32 MiB array (the scratch of sgemm_streamk_static()); every process that
+ * initialises a device with any entry point holds it on that device until it
+ * exits, whether or not it ever calls sgemm_streamk_static().
  *
  * Errors.  Every entry point returns an sgemm_status_t and never aborts the
  * process.  Argument errors are found on the host before any launch.  A
@@ -170,14 +178,23 @@ sgemm_status_t sgemm_tf32(int64_t M, int64_t N, int64_t K, const float *A, int64
                           const float *B, int64_t ldb, float *C, int64_t ldc, cudaStream_t stream);
 
 /*
- * Reads, then clears, the device status word of the current device after
- * synchronising `stream`: SGEMM_OK, or SGEMM_ERR_TIMEOUT if a kernel gave up
- * waiting since the last query.  *detail (may be NULL) receives a code that
- * says which wait expired (0 when none).
+ * Reads, then clears, the device status word of the current device: the read
+ * is queued on `stream` (an atomic exchange on the device), and the call
+ * returns once `stream` has reached it.  Returns SGEMM_OK, or
+ * SGEMM_ERR_TIMEOUT if a kernel gave up waiting since the last query.
+ * *detail (may be NULL) receives a code that says which wait expired (0 when
+ * none).  After a timeout the split-K arrival counters of every cached
+ * workspace of the device may be stale: each is cleared on its own stream,
+ * in stream order, before that stream's next call uses it, so kernels still
+ * running on other streams are not disturbed.
  */
 sgemm_status_t sgemm_query_device_status(cudaStream_t stream, uint32_t *detail);
 
-/* Frees every cached workspace of every device (synchronises the device first). */
+/*
+ * Frees every cached workspace of every device, including those replaced by
+ * larger ones (synchronises each device first).  CUDA graphs captured with
+ * sgemm() calls must not be replayed afterwards.
+ */
 void sgemm_release_workspaces(void);
 
 /* Static description of a status code; never NULL. */
@@ -197,10 +214,10 @@ sgemm_status_t sgemm_debug_expire_wait(uint64_t limit_ns, cudaStream_t stream);
 /*
  * C = A * B with the Stream-K schedule (SGEMM_VARIANT_STREAMK), allocating
  * nothing.  The pages have no counterpart: this entry point exists for
- * callers that cannot let a library call cudaMalloc -- code that runs while
- * its stream is being captured, code that must never wait on the whole
- * device (cudaMalloc and cudaFree may synchronise it), and code that hands
- * out a fixed memory budget before any work starts.
+ * callers that cannot let a library call cudaMalloc -- code that must never
+ * wait on the whole device (cudaMalloc and cudaFree may synchronise it), code
+ * that hands out a fixed memory budget before any work starts, and code
+ * inside a framework whose own allocator owns the device memory.
  *
  * Arguments, layout and ownership are those of sgemm().  The Stream-K
  * scratch (arrival counters and partial sums of split tiles) lives in one

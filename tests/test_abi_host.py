@@ -77,9 +77,24 @@ def test_invalid_arguments_rejected(lib, args):
     assert lib.sgemm_select_variant(*args) == -1
 
 
-def test_unknown_variant_rejected(lib):
-    assert binding.sgemm_raw(4, 4, 4, P_A, 4, P_B, 4, P_C, 4, variant=7) in (
-        binding.ERR_INVALID_VALUE, binding.ERR_UNSUPPORTED)
+def _header_constant(name):
+    text = open(os.path.join(ROOT, "include", "sgemm.h")).read()
+    return int(re.search(rf"\b{name}\s*=\s*(-?\d+)", text).group(1))
+
+
+# One past the last variant id, as the header declares it.
+VARIANT_COUNT = _header_constant("SGEMM_VARIANT_COUNT")
+
+
+def test_variant_ids_cover_the_header_enum():
+    assert sorted(binding.VARIANTS.values()) == list(range(VARIANT_COUNT))
+
+
+@pytest.mark.parametrize("variant", [VARIANT_COUNT, -2, 1000])
+def test_unknown_variant_rejected(lib, variant):
+    """The range check runs before any device is touched, so the status is exact here."""
+    assert binding.sgemm_raw(4, 4, 4, P_A, 4, P_B, 4, P_C, 4, variant=variant) == \
+        binding.ERR_INVALID_VALUE
 
 
 def test_oversized_dimension_unsupported(lib):

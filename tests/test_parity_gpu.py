@@ -335,3 +335,76 @@ def test_graph_capture_and_replay():
     torch.cuda.synchronize()
     ref, E = oracle.sgemm_f64(A.cpu(), B_h)
     check_within_bound(C.cpu().numpy(), ref, E, w.K, "graph replay")
+
+
+def test_graph_replay_after_workspace_regrowth():
+    """A graph captured with sgemm() keeps a valid workspace after a larger call on the
+    same stream replaced the stream's cached workspace (the old one is retired, not freed)."""
+    w = workloads.SQUARE_1024
+    A_h, B_h = workloads.operands(w)
+    A, B = A_h.cuda(), B_h.cuda()
+    C = torch.empty(w.M, w.N, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        sg.sgemm(A, B, out=C)
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        sg.sgemm(A, B, out=C)
+    # A product whose split tiles need more workspace than 1024^3 left in the cache.
+    big = next(x for x in workloads.SWEEP if x.M == 1536)
+    assert sg.workspace_size(big.M, big.N, big.K) > 1.25 * sg.workspace_size(w.M, w.N, w.K)
+    Ab, Bb = (x.cuda() for x in workloads.operands(big))
+    with torch.cuda.stream(s):
+        Cb = sg.sgemm(Ab, Bb)
+    s.synchronize()
+    C.fill_(float("nan"))
+    A.copy_(workloads.matrix(w.M, w.K, w.dist, 4343, 0))
+    graph.replay()
+    torch.cuda.synchronize()
+    ref, E = oracle.sgemm_f64(A.cpu(), B_h)
+    check_within_bound(C.cpu().numpy(), ref, E, w.K, "graph replay after regrowth")
+    r, c = workloads.sample_indices(big.M, big.N, 1024, big.seed)
+    ref_b, E_b = oracle.sgemm_entries_f64(*workloads.operands(big), r.numpy(), c.numpy())
+    check_within_bound(Cb[r.cuda(), c.cuda()].cpu().numpy(), ref_b, E_b, big.K, "regrown call")
+
+
+def test_unknown_variant_rejected_on_a_device():
+    A = torch.ones(64, 64, device="cuda")
+    C = torch.full((64, 64), 7.0, device="cuda")
+    for v in (len(sg.VARIANTS), -2):
+        with pytest.raises(sg.SgemmError) as e:
+            sg.sgemm(A, A, out=C, variant=v)
+        assert e.value.status == sg.binding.ERR_INVALID_VALUE
+    torch.cuda.synchronize()
+    assert bool((C == 7.0).all())
+
+
+def test_timeout_on_one_stream_leaves_other_streams_running():
+    """A wait that expires on one stream while Stream-K calls run on another: the query
+    that reports it must not clear the other stream's workspace under its kernels.  The
+    other stream's results, and its next call, must still be exact."""
+    w = workloads.SQUARE_1024
+    A_h, B_h = workloads.operands(w)
+    A, B = A_h.cuda(), B_h.cuda()
+    s_probe, s_work = torch.cuda.Stream(), torch.cuda.Stream()
+    with torch.cuda.stream(s_work):
+        first = sg.sgemm(A, B, variant=sg.STREAMK_SMALL)   # sizes s_work's workspace
+    s_work.synchronize()
+    outs = [torch.full((w.M, w.N), float("nan"), device="cuda") for _ in range(40)]
+    with torch.cuda.stream(s_work):
+        torch.cuda._sleep(2_000_000)      # about 1 ms: the calls below start after the probe
+        for out in outs:
+            sg.sgemm(A, B, out=out, variant=sg.STREAMK_SMALL)
+    assert sg.debug_expire_wait(2_000_000, stream=s_probe) == 0   # expires after 2 ms
+    st, site = sg.query_device_status(stream=s_probe)               # while s_work still runs
+    assert (st, site) == (3, 3)
+    with torch.cuda.stream(s_work):
+        after = sg.sgemm(A, B, variant=sg.STREAMK_SMALL)          # counters cleared first
+    torch.cuda.synchronize()
+    for i, out in enumerate(outs):
+        assert torch.equal(out, first), f"call {i} on the other stream changed"
+    assert torch.equal(after, first)
+    ref, E = oracle.sgemm_f64(A_h, B_h)
+    check_within_bound(first.cpu().numpy(), ref, E, w.K, "stream-K beside an expiring wait")
+    assert sg.query_device_status() == (0, 0)

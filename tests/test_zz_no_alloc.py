@@ -1,16 +1,18 @@
 """The allocation-free Stream-K entry point, ``sgemm_streamk_static``.
 
-Some callers cannot let a library allocate device memory: code running while
-its stream is being captured, code that must never wait on the whole device
-(cudaMalloc and cudaFree may synchronise it), and code with a memory budget
-fixed before work starts.  For them the library keeps the Stream-K scratch
-in one fixed array in its device image and this entry point uses only that.
+Some callers cannot let a library allocate device memory: code that must
+never wait on the whole device (cudaMalloc and cudaFree may synchronise it),
+code with a memory budget fixed before work starts, and code inside a
+framework whose own allocator owns the device memory.  For them the library
+keeps the Stream-K scratch in one fixed array in its device image and this
+entry point uses only that.
 
-The test calls it through the C ABI twice in a row on shapes whose Stream-K
+The tests call it through the C ABI twice in a row on shapes whose Stream-K
 schedule splits tiles (so the array's counters and partial sums are used and
-reused), and checks each result against the regular entry point's result
-within the parity tolerance of the other GPU tests, 4 K 2^-24 sum_k |A B|.
-It runs last (file name) so that a failure here leaves every other test run.
+reused), check each result against the regular entry point's result within
+the parity tolerance of the other GPU tests, 4 K 2^-24 sum_k |A B|, and check
+that the device's free memory does not change across such calls.  The file
+runs last (file name) so that a failure here leaves every other test run.
 """
 import numpy as np
 import pytest
@@ -77,3 +79,29 @@ def test_static_scratch_rejects_shapes_beyond_the_array():
     assert _static_call(A, B, C) == sg.binding.ERR_UNSUPPORTED
     torch.cuda.synchronize()
     assert bool((C == 7.0).all())
+
+
+def test_static_calls_leave_device_memory_unchanged():
+    """Two calls after the first (which looks up the array's address) change the device's
+    free memory by nothing: the library allocates no device memory on this path."""
+    shapes = [(1024, 1024, 1024, 73), (768, 1280, 1536, 74)]
+    ops = []
+    for M, N, K, seed in shapes:
+        A_h = workloads.matrix(M, K, "normal", seed, 0)
+        B_h = workloads.matrix(K, N, "normal", seed, 1)
+        ops.append((A_h, B_h, A_h.cuda(), B_h.cuda(), torch.full((M, N), float("nan"), device="cuda")))
+    A0, B0, C0 = ops[0][2], ops[0][3], ops[0][4]
+    assert _static_call(A0, B0, C0) == sg.binding.OK      # set-up on this device
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    for _, _, A, B, C in ops:
+        C.fill_(float("nan"))
+    torch.cuda.synchronize()
+    for _, _, A, B, C in ops:
+        assert _static_call(A, B, C) == sg.binding.OK
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free_before
+    assert sg.query_device_status() == (0, 0)
+    for (A_h, B_h, _, _, C), (M, N, K, _) in zip(ops, shapes):
+        ref, E = oracle.sgemm_f64(A_h, B_h)
+        check_within_bound(C.cpu().numpy(), ref, E, K, f"static scratch, no allocation {(M, N, K)}")
