@@ -25,7 +25,7 @@ VARIANTS = {"guarded": GUARDED, "tiled": TILED, "streamk": STREAMK,
 EXPORTS = ("sgemm", "sgemm_variant", "sgemm_select_variant", "sgemm_workspace_size",
            "sgemm_query_device_status", "sgemm_release_workspaces", "sgemm_status_string",
            "sgemm_variant_name", "sgemm_debug_expire_wait", "sgemm_streamk_static",
-           "sgemm_tf32", "sgemm_ex")
+           "sgemm_tf32", "sgemm_ex", "sgemm_ex2")
 
 
 class SgemmError(RuntimeError):
@@ -82,6 +82,9 @@ def load(path: str | None = None):
         f32 = ctypes.c_float
         lib.sgemm_ex.argtypes = [ctypes.c_int, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
         lib.sgemm_ex.restype = st
+        lib.sgemm_ex2.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, i64, i64, f32, vp,
+                                  i64, vp, i64, f32, vp, i64, vp]
+        lib.sgemm_ex2.restype = st
         _lib = lib
         return lib
 
@@ -183,6 +186,43 @@ def sgemm_ex(A, B, C, alpha=1.0, beta=0.0, layout=ROW_MAJOR, stream=None):
                              _stream_handle(A.device, stream))
     if st != OK:
         raise SgemmError(st, "sgemm_ex")
+    return C
+
+
+OP_N, OP_T = 0, 1
+
+
+def sgemm_ex2(A, B, C, alpha=1.0, beta=0.0, trans_a=False, trans_b=False, layout=ROW_MAJOR,
+              stream=None):
+    """C = alpha * op(A) @ op(B) + beta * C in place; op(X) = X.T when trans_x.
+
+    ``A`` and ``B`` are the stored matrices: A is M x K (K x M when
+    ``trans_a``), B is K x N (N x K when ``trans_b``); C is M x N.  Storage
+    order as for :func:`sgemm_ex` (``layout``).
+    """
+    import torch
+
+    def ld(t, name):
+        if t.device.type != "cuda" or t.dtype != torch.float32 or t.dim() != 2:
+            raise ValueError(f"{name} must be a 2-D float32 CUDA tensor")
+        if layout == ROW_MAJOR:
+            if t.shape[1] > 1 and t.stride(1) != 1:
+                raise ValueError(f"{name} must have unit column stride")
+            return max(t.stride(0), t.shape[1], 1)
+        if t.shape[0] > 1 and t.stride(0) != 1:
+            raise ValueError(f"{name} must have unit row stride")
+        return max(t.stride(1), t.shape[0], 1)
+    lda, ldb, ldc = ld(A, "A"), ld(B, "B"), ld(C, "C")
+    M, K = (A.shape[1], A.shape[0]) if trans_a else tuple(A.shape)
+    K2, N = (B.shape[1], B.shape[0]) if trans_b else tuple(B.shape)
+    if K != K2 or tuple(C.shape) != (M, N):
+        raise ValueError(f"shapes do not match: op(A) {M}x{K}, op(B) {K2}x{N}, C {tuple(C.shape)}")
+    with torch.cuda.device(A.device):
+        st = load().sgemm_ex2(int(layout), OP_T if trans_a else OP_N, OP_T if trans_b else OP_N,
+                              M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb,
+                              float(beta), C.data_ptr(), ldc, _stream_handle(A.device, stream))
+    if st != OK:
+        raise SgemmError(st, "sgemm_ex2")
     return C
 
 

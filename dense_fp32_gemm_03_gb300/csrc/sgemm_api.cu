@@ -169,17 +169,27 @@ bool overlaps(const float* a, int64_t rows, int64_t cols, int64_t ld, const floa
   return a0 < c1 && c0 < a1;
 }
 
-sgemm_status_t validate(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
-                        const float* B, int64_t ldb, const float* C, int64_t ldc) {
+// Argument checks.  A holds op(A) (M x K) or, when trans_a, op(A)^T (K x M);
+// B holds op(B) (K x N) or, when trans_b, op(B)^T (N x K); row strides lda,
+// ldb, ldc cover the stored rows.
+sgemm_status_t validate(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, bool trans_a,
+                        const float* B, int64_t ldb, bool trans_b, const float* C, int64_t ldc) {
   if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_VALUE;
   if (M > kInt32Max || N > kInt32Max || K > kInt32Max) return SGEMM_ERR_UNSUPPORTED;
   if (M == 0 || N == 0) return SGEMM_OK;
   if (C == nullptr || ldc < N) return SGEMM_ERR_INVALID_VALUE;
   if (K == 0) return SGEMM_OK;
-  if (A == nullptr || B == nullptr || lda < K || ldb < N) return SGEMM_ERR_INVALID_VALUE;
-  if (overlaps(A, M, K, lda, C, M, N, ldc) || overlaps(B, K, N, ldb, C, M, N, ldc))
+  const int64_t a_rows = trans_a ? K : M, a_cols = trans_a ? M : K;
+  const int64_t b_rows = trans_b ? N : K, b_cols = trans_b ? K : N;
+  if (A == nullptr || B == nullptr || lda < a_cols || ldb < b_cols) return SGEMM_ERR_INVALID_VALUE;
+  if (overlaps(A, a_rows, a_cols, lda, C, M, N, ldc) || overlaps(B, b_rows, b_cols, ldb, C, M, N, ldc))
     return SGEMM_ERR_INVALID_VALUE;
   return SGEMM_OK;
+}
+
+sgemm_status_t validate(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+                        const float* B, int64_t ldb, const float* C, int64_t ldc) {
+  return validate(M, N, K, A, lda, false, B, ldb, false, C, ldc);
 }
 
 bool fast_path_ok(const float* A, int64_t lda, const float* B, int64_t ldb, const float* C,
@@ -371,18 +381,54 @@ double guarded_cost_us(int64_t M, int64_t N, int64_t K, const DeviceState& ds) {
   return 5.0 + (latency > arithmetic ? latency : arithmetic);
 }
 
-// Estimated cost (microseconds) of copying the operands that need it: one
-// launch, then 8 bytes of traffic per element.
-double staging_cost_us(int64_t M, int64_t N, int64_t K, bool stage_a, bool stage_b) {
-  if (!stage_a && !stage_b) return 0.0;
-  double elems = 0.0;
-  if (stage_a) elems += double(M) * double(K);
-  if (stage_b) elems += double(K) * double(N);
-  return 4.0 + 8.0 * elems / kCopyBytesPerUs;
+// How a fast variant receives an operand.
+enum OpMode {
+  kInPlace,    // read where it is (16-byte aligned, row stride a multiple of 4)
+  kInPlaceMN,  // A^T read where it is as an M-major A (pipelined kernels only)
+  kPack,       // copied into the workspace as is, aligned (pack_kernel)
+  kTranspose,  // copied into the workspace transposed (transpose kernel)
+};
+
+bool reads_a_mn(int v) {
+  return v == SGEMM_VARIANT_TILED || v == SGEMM_VARIANT_STREAMK || v == SGEMM_VARIANT_TILED_SMALL ||
+         v == SGEMM_VARIANT_STREAMK_SMALL;
 }
 
-// The pipelined variant with the lowest estimated time for this shape.
-int select_fast(int64_t M, int64_t N, int64_t K, const DeviceState& ds, double* cost_out) {
+OpMode a_mode(int v, bool trans_a, bool aligned) {
+  if (!trans_a) return aligned ? kInPlace : kPack;
+  return aligned && reads_a_mn(v) ? kInPlaceMN : kTranspose;
+}
+
+OpMode b_mode(bool trans_b, bool aligned) {
+  if (!trans_b) return aligned ? kInPlace : kPack;
+  return kTranspose;
+}
+
+bool is_copy(OpMode m) { return m == kPack || m == kTranspose; }
+
+// Estimated cost (microseconds) of the operand copies: 8 bytes of traffic per
+// element, plus a launch for the packed copies (one for both) and one per
+// transposed copy.
+double copies_cost_us(int64_t M, int64_t N, int64_t K, OpMode am, OpMode bm) {
+  double us = 0.0;
+  int launches = 0;
+  bool pack = false;
+  if (is_copy(am)) {
+    us += 8.0 * double(M) * double(K) / kCopyBytesPerUs;
+    if (am == kTranspose) ++launches; else pack = true;
+  }
+  if (is_copy(bm)) {
+    us += 8.0 * double(K) * double(N) / kCopyBytesPerUs;
+    if (bm == kTranspose) ++launches; else pack = true;
+  }
+  if (pack) ++launches;
+  return us + 4.0 * launches;
+}
+
+// The pipelined variant with the lowest estimated time for this shape,
+// operand copies included (a_ok, b_ok: the operand could be read in place).
+int select_fast(int64_t M, int64_t N, int64_t K, bool trans_a, bool a_ok, bool trans_b, bool b_ok,
+                const DeviceState& ds, double* cost_out) {
   int best = SGEMM_VARIANT_STREAMK;
   double best_cost = 1e300;
   const int candidates[5] = {SGEMM_VARIANT_STREAMK, SGEMM_VARIANT_STREAMK_SMALL,
@@ -390,7 +436,8 @@ int select_fast(int64_t M, int64_t N, int64_t K, const DeviceState& ds, double* 
   for (int v : candidates) {
     Plan p;
     if (!make_plan(v, M, N, K, ds, &p)) continue;
-    const double cost = plan_cost_us(p, ds);
+    const double cost = plan_cost_us(p, ds) +
+                        copies_cost_us(M, N, K, a_mode(v, trans_a, a_ok), b_mode(trans_b, b_ok));
     if (cost < best_cost * 0.999) {
       best_cost = cost;
       best = v;
@@ -400,22 +447,35 @@ int select_fast(int64_t M, int64_t N, int64_t K, const DeviceState& ds, double* 
   return best;
 }
 
-// The selector: aligned operands take the pipelined variant with the lowest
-// estimated time; the rest take the staged variant or the bounds-checked
-// kernel, whichever is estimated faster.
-int select_variant(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
-                   int64_t ldb, const float* C, int64_t ldc, const DeviceState& ds) {
+int select_fast(int64_t M, int64_t N, int64_t K, const DeviceState& ds, double* cost_out) {
+  return select_fast(M, N, K, false, true, false, true, ds, cost_out);
+}
+
+// The selector: when every operand a pipelined kernel reads in place is
+// aligned (a transposed B is always copied; a transposed A is read M-major
+// where it is, or copied), the pipelined variant with the lowest estimated
+// time; otherwise the staged variant or the bounds-checked kernel, whichever
+// is estimated faster.
+int select_variant(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, bool trans_a,
+                   const float* B, int64_t ldb, bool trans_b, const float* C, int64_t ldc,
+                   const DeviceState& ds) {
+  const bool a_ok = operand_ok(A, lda), b_ok = operand_ok(B, ldb), c_ok = operand_ok(C, ldc);
   double cost = 0.0;
-  const int fast = select_fast(M, N, K, ds, &cost);
-  if (fast_path_ok(A, lda, B, ldb, C, ldc)) {
+  const int fast = select_fast(M, N, K, trans_a, a_ok, trans_b, b_ok, ds, &cost);
+  if (c_ok && (a_ok || trans_a) && (b_ok || trans_b)) {
     Plan p;
-    if (make_plan(fast, M, N, K, ds, &p) && find_specialized(p, M, N, K, ds) >= 0)
+    const OpMode am = a_mode(fast, trans_a, a_ok);
+    if (!is_copy(am) && !trans_b && make_plan(fast, M, N, K, ds, &p) &&
+        find_specialized(p, M, N, K, ds) >= 0)
       return SGEMM_VARIANT_SPECIALIZED;
     return fast;
   }
-  const double staged =
-      cost + staging_cost_us(M, N, K, !operand_ok(A, lda), !operand_ok(B, ldb));
-  return staged < guarded_cost_us(M, N, K, ds) ? SGEMM_VARIANT_STAGED : SGEMM_VARIANT_GUARDED;
+  return cost < guarded_cost_us(M, N, K, ds) ? SGEMM_VARIANT_STAGED : SGEMM_VARIANT_GUARDED;
+}
+
+int select_variant(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda, const float* B,
+                   int64_t ldb, const float* C, int64_t ldc, const DeviceState& ds) {
+  return select_variant(M, N, K, A, lda, false, B, ldb, false, C, ldc, ds);
 }
 
 sgemm_status_t get_workspace_bytes(int dev, cudaStream_t stream, size_t need, void** out) {
@@ -457,19 +517,23 @@ sgemm_status_t get_workspace_bytes(int dev, cudaStream_t stream, size_t need, vo
 }
 
 // Tensor maps of the pipelined kernel: A (K fastest) in boxes of 16 x
-// a_box_rows with the 64-byte swizzle, B (N fastest) in boxes of BN x 16.
+// a_box_rows with the 64-byte swizzle, or, for an M-major A (a_mn: the
+// storage of A^T, K x M with M fastest), boxes of BM x 16 without swizzle;
+// B (N fastest) in boxes of BN x 16.
 sgemm_status_t encode_operands(const TileShape& ts, int64_t M, int64_t N, int64_t K, const float* A,
-                               int64_t lda, const float* B, int64_t ldb, CUtensorMap* tmap_a,
-                               CUtensorMap* tmap_b) {
+                               int64_t lda, bool a_mn, const float* B, int64_t ldb,
+                               CUtensorMap* tmap_a, CUtensorMap* tmap_b) {
   std::memset(tmap_a, 0, sizeof(*tmap_a));
   std::memset(tmap_b, 0, sizeof(*tmap_b));
   const cuuint32_t estr[2] = {1, 1};
   {
-    const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(M)};
+    const cuuint64_t dims[2] = {a_mn ? cuuint64_t(M) : cuuint64_t(K), a_mn ? cuuint64_t(K) : cuuint64_t(M)};
     const cuuint64_t strides[1] = {cuuint64_t(lda) * 4};
-    const cuuint32_t box[2] = {cuuint32_t(ts.bk), cuuint32_t(ts.a_box_rows)};
+    const cuuint32_t box[2] = {a_mn ? cuuint32_t(ts.bm) : cuuint32_t(ts.bk),
+                               a_mn ? cuuint32_t(ts.bk) : cuuint32_t(ts.a_box_rows)};
     if (g_encode(tmap_a, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(A), dims, strides,
-                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 a_mn ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_64B,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return SGEMM_ERR_LAUNCH;
   }
@@ -485,11 +549,13 @@ sgemm_status_t encode_operands(const TileShape& ts, int64_t M, int64_t N, int64_
   return SGEMM_OK;
 }
 
+// One call of the product C = alpha * op(A) op(B) + beta * C in row-major
+// storage (trans_a / trans_b: the operand is stored transposed).
 sgemm_status_t run(int variant, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
-                   int64_t lda, const float* B, int64_t ldb, float beta, float* C, int64_t ldc,
-                   cudaStream_t stream) {
+                   int64_t lda, bool trans_a, const float* B, int64_t ldb, bool trans_b, float beta,
+                   float* C, int64_t ldc, cudaStream_t stream) {
   const bool scaled = !(alpha == 1.0f && beta == 0.0f);
-  sgemm_status_t st = validate(M, N, K, A, lda, B, ldb, C, ldc);
+  sgemm_status_t st = validate(M, N, K, A, lda, trans_a, B, ldb, trans_b, C, ldc);
   if (st != SGEMM_OK) return st;
   if (variant < SGEMM_VARIANT_AUTO || variant >= SGEMM_VARIANT_COUNT) return SGEMM_ERR_INVALID_VALUE;
   DeviceState* ds = nullptr;
@@ -502,32 +568,35 @@ sgemm_status_t run(int variant, int64_t M, int64_t N, int64_t K, float alpha, co
                                  : gb300::launch_zero_fill(M, N, C, ldc, stream);
     return e == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
   }
-  if (variant == SGEMM_VARIANT_AUTO) variant = select_variant(M, N, K, A, lda, B, ldb, C, ldc, *ds);
+  if (variant == SGEMM_VARIANT_AUTO)
+    variant = select_variant(M, N, K, A, lda, trans_a, B, ldb, trans_b, C, ldc, *ds);
   if (variant == SGEMM_VARIANT_GUARDED) {
-    return gb300::launch_guarded_kernel(M, N, K, A, lda, B, ldb, C, ldc, scaled ? 1 : 0, alpha,
-                                        beta, stream) == cudaSuccess
+    return gb300::launch_guarded_kernel(M, N, K, A, lda, trans_a, B, ldb, trans_b, C, ldc,
+                                        scaled ? 1 : 0, alpha, beta, stream) == cudaSuccess
                ? SGEMM_OK
                : SGEMM_ERR_LAUNCH;
   }
+  const bool a_ok = operand_ok(A, lda), b_ok = operand_ok(B, ldb), c_ok = operand_ok(C, ldc);
   const bool staged = variant == SGEMM_VARIANT_STAGED;
   const bool specialized = variant == SGEMM_VARIANT_SPECIALIZED;
   if (staged || specialized)
-    variant = select_fast(M, N, K, *ds, nullptr);
-  if (!staged && !fast_path_ok(A, lda, B, ldb, C, ldc)) return SGEMM_ERR_INVALID_VALUE;
+    variant = select_fast(M, N, K, trans_a, a_ok, trans_b, b_ok, *ds, nullptr);
+  const OpMode am = a_mode(variant, trans_a, a_ok), bm = b_mode(trans_b, b_ok);
+  // Outside the staged variant, operands are only copied to transpose them.
+  if (!staged && (am == kPack || bm == kPack || !c_ok)) return SGEMM_ERR_INVALID_VALUE;
   Plan p;
   if (!make_plan(variant, M, N, K, *ds, &p)) return SGEMM_ERR_UNSUPPORTED;
-  // The compiled-in schedule serves the plain epilogue only; the selector
-  // names it for any shape it fits, so alpha / beta fall back to the generic
-  // instance of the same schedule.
+  // The compiled-in schedule serves the plain epilogue over operands read in
+  // place; the selector names it for any shape it fits, so alpha / beta fall
+  // back to the generic instance of the same schedule.
   int spec = -1;
   if (specialized) {
     spec = find_specialized(p, M, N, K, *ds);
-    if (spec < 0) return SGEMM_ERR_UNSUPPORTED;
+    if (spec < 0 || is_copy(am) || is_copy(bm)) return SGEMM_ERR_UNSUPPORTED;
     if (scaled) spec = -1;
   }
   const TileShape ts = gb300::tile_shape(p.cfg);
-  const Staging sg =
-      make_staging(p, M, N, K, staged && !operand_ok(A, lda), staged && !operand_ok(B, ldb));
+  const Staging sg = make_staging(p, M, N, K, is_copy(am), is_copy(bm));
 
   void* ws = nullptr;
   st = get_workspace_bytes(dev, stream, sg.bytes, &ws);
@@ -538,17 +607,29 @@ sgemm_status_t run(int variant, int64_t M, int64_t N, int64_t K, float alpha, co
   gb300::PackCopy copy_a{}, copy_b{};
   if (sg.a) {
     float* a_copy = reinterpret_cast<float*>(static_cast<char*>(ws) + sg.a_off);
-    copy_a = gb300::PackCopy{A, a_copy, M, K, lda, sg.lda};
+    if (am == kTranspose) {
+      // A holds op(A)^T (K x M): its transpose is the row-major M x K op(A).
+      if (gb300::launch_transpose(A, lda, a_copy, sg.lda, int(K), int(M), stream) != cudaSuccess)
+        return SGEMM_ERR_LAUNCH;
+    } else {
+      copy_a = gb300::PackCopy{A, a_copy, M, K, lda, sg.lda};
+    }
     a_in = a_copy;
     lda_in = sg.lda;
   }
   if (sg.b) {
     float* b_copy = reinterpret_cast<float*>(static_cast<char*>(ws) + sg.b_off);
-    copy_b = gb300::PackCopy{B, b_copy, K, N, ldb, sg.ldb};
+    if (bm == kTranspose) {
+      // B holds op(B)^T (N x K): its transpose is the row-major K x N op(B).
+      if (gb300::launch_transpose(B, ldb, b_copy, sg.ldb, int(N), int(K), stream) != cudaSuccess)
+        return SGEMM_ERR_LAUNCH;
+    } else {
+      copy_b = gb300::PackCopy{B, b_copy, K, N, ldb, sg.ldb};
+    }
     b_in = b_copy;
     ldb_in = sg.ldb;
   }
-  if ((sg.a || sg.b) && gb300::launch_pack(copy_a, copy_b, stream) != cudaSuccess)
+  if ((am == kPack || bm == kPack) && gb300::launch_pack(copy_a, copy_b, stream) != cudaSuccess)
     return SGEMM_ERR_LAUNCH;
   if (p.variant == SGEMM_VARIANT_SMALL) {
     gb300::SmallArgs sa{};
@@ -569,12 +650,13 @@ sgemm_status_t run(int variant, int64_t M, int64_t N, int64_t K, float alpha, co
     sa.scaled = scaled ? 1 : 0;
     sa.alpha = alpha;
     sa.beta = beta;
-    sa.c_scalar = operand_ok(C, ldc) ? 0 : 1;
+    sa.c_scalar = c_ok ? 0 : 1;
     return gb300::launch_small_kernel(sa, p.small_tiles, stream) == cudaSuccess ? SGEMM_OK
                                                                                : SGEMM_ERR_LAUNCH;
   }
+  const bool a_mn = am == kInPlaceMN;
   CUtensorMap tmap_a, tmap_b;
-  st = encode_operands(ts, M, N, K, a_in, lda_in, b_in, ldb_in, &tmap_a, &tmap_b);
+  st = encode_operands(ts, M, N, K, a_in, lda_in, a_mn, b_in, ldb_in, &tmap_a, &tmap_b);
   if (st != SGEMM_OK) return st;
 
   gb300::GemmArgs args{};
@@ -592,11 +674,18 @@ sgemm_status_t run(int variant, int64_t M, int64_t N, int64_t K, float alpha, co
   args.scaled = scaled ? 1 : 0;
   args.alpha = alpha;
   args.beta = beta;
-  args.c_scalar = operand_ok(C, ldc) ? 0 : 1;
+  args.c_scalar = c_ok ? 0 : 1;
+  args.a_mn = a_mn ? 1 : 0;
   const cudaError_t e =
       spec >= 0 ? gb300::launch_specialized(spec, tmap_a, tmap_b, args, p.sc, p.grid, stream)
                 : gb300::launch_tile_kernel(p.cfg, tmap_a, tmap_b, args, p.sc, p.grid, stream);
   return e == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+}
+
+sgemm_status_t run(int variant, int64_t M, int64_t N, int64_t K, float alpha, const float* A,
+                   int64_t lda, const float* B, int64_t ldb, float beta, float* C, int64_t ldc,
+                   cudaStream_t stream) {
+  return run(variant, M, N, K, alpha, A, lda, false, B, ldb, false, beta, C, ldc, stream);
 }
 
 }  // namespace
@@ -617,6 +706,23 @@ sgemm_status_t sgemm_ex(int layout, int64_t M, int64_t N, int64_t K, float alpha
   // Column-major C = A B is row-major C^T = B^T A^T over the same memory: the
   // column-major B (K x N, ld ldb) read row-major is B^T (N x K), and so on.
   return run(SGEMM_VARIANT_AUTO, N, M, K, alpha, B, ldb, A, lda, beta, C, ldc, stream);
+}
+
+sgemm_status_t sgemm_ex2(int layout, int trans_a, int trans_b, int64_t M, int64_t N, int64_t K,
+                         float alpha, const float* A, int64_t lda, const float* B, int64_t ldb,
+                         float beta, float* C, int64_t ldc, cudaStream_t stream) {
+  if ((trans_a != SGEMM_OP_N && trans_a != SGEMM_OP_T) ||
+      (trans_b != SGEMM_OP_N && trans_b != SGEMM_OP_T))
+    return SGEMM_ERR_INVALID_VALUE;
+  const bool ta = trans_a == SGEMM_OP_T, tb = trans_b == SGEMM_OP_T;
+  if (layout == SGEMM_ROW_MAJOR)
+    return run(SGEMM_VARIANT_AUTO, M, N, K, alpha, A, lda, ta, B, ldb, tb, beta, C, ldc, stream);
+  if (layout != SGEMM_COL_MAJOR) return SGEMM_ERR_INVALID_VALUE;
+  // Column-major C = op(A) op(B) is row-major C^T = op(B)^T op(A)^T over the
+  // same memory.  A column-major matrix read row-major is its transpose, so
+  // B's memory read row-major is op(B)^T exactly when op(B) = B (trans_b ==
+  // N): each operand keeps its own flag.
+  return run(SGEMM_VARIANT_AUTO, N, M, K, alpha, B, ldb, tb, A, lda, ta, beta, C, ldc, stream);
 }
 
 sgemm_status_t sgemm_variant(int variant, int64_t M, int64_t N, int64_t K, const float* A,
@@ -917,7 +1023,7 @@ extern "C" sgemm_status_t sgemm_streamk_static(int64_t M, int64_t N, int64_t K, 
   const TileShape ts = gb300::tile_shape(p.cfg);
 
   CUtensorMap tmap_a, tmap_b;
-  st = encode_operands(ts, M, N, K, A, lda, B, ldb, &tmap_a, &tmap_b);
+  st = encode_operands(ts, M, N, K, A, lda, false, B, ldb, &tmap_a, &tmap_b);
   if (st != SGEMM_OK) return st;
 
   // The array keeps whatever the previous call left: the arrival counters of

@@ -19,11 +19,14 @@ constexpr int kGBM = 64, kGBN = 64, kGBK = 16, kGThreads = 256;
 // Block Tiling: Scaling Matrix Multiplication on NVIDIA H100", section 5, the
 // edge kernel), correct for every shape, stride and alignment.  Each thread
 // computes a 4 x 4 patch whose rows and columns are strided by 16, so that the
-// shared-memory reads of a warp fall in distinct banks or broadcast.
+// shared-memory reads of a warp fall in distinct banks or broadcast.  op(A)
+// element (m, k) is read at A[m * a_m + k * a_k] and op(B) element (k, n) at
+// B[k * b_k + n * b_n], so one kernel serves stored and transposed operands.
 __global__ void __launch_bounds__(kGThreads)
-    guarded_kernel(int64_t M, int64_t N, int64_t K, const float* __restrict__ A, int64_t lda,
-                   const float* __restrict__ B, int64_t ldb, float* __restrict__ C, int64_t ldc,
-                   int64_t tiles_n, int scaled, float alpha, float beta) {
+    guarded_kernel(int64_t M, int64_t N, int64_t K, const float* __restrict__ A, int64_t a_m,
+                   int64_t a_k, const float* __restrict__ B, int64_t b_k, int64_t b_n,
+                   float* __restrict__ C, int64_t ldc, int64_t tiles_n, int scaled, float alpha,
+                   float beta) {
   __shared__ float As[kGBK][kGBM];
   __shared__ float Bs[kGBK][kGBN];
   const int64_t tile = blockIdx.x;
@@ -36,14 +39,14 @@ __global__ void __launch_bounds__(kGThreads)
       const int idx = tid + e * kGThreads;
       const int r = idx / kGBK, kk = idx % kGBK;
       const int64_t gm = m0 + r, gk = k0 + kk;
-      As[kk][r] = (gm < M && gk < K) ? A[gm * lda + gk] : 0.f;
+      As[kk][r] = (gm < M && gk < K) ? A[gm * a_m + gk * a_k] : 0.f;
     }
 #pragma unroll
     for (int e = 0; e < kGBN * kGBK / kGThreads; ++e) {
       const int idx = tid + e * kGThreads;
       const int kk = idx / kGBN, c = idx % kGBN;
       const int64_t gk = k0 + kk, gn = n0 + c;
-      Bs[kk][c] = (gk < K && gn < N) ? B[gk * ldb + gn] : 0.f;
+      Bs[kk][c] = (gk < K && gn < N) ? B[gk * b_k + gn * b_n] : 0.f;
     }
     __syncthreads();
 #pragma unroll
@@ -133,8 +136,6 @@ __global__ void scale_kernel(int64_t M, int64_t N, float* __restrict__ C, int64_
   }
 }
 
-// One CTA waits on a barrier that nothing completes; the bounded wait gives up
-// after limit_ns and the timeout is recorded.  Nothing is in flight.
 // Moves the live status word (status[0..1]) into the snapshot (status[2..3])
 // and clears it, atomically with respect to kernels still recording on other
 // streams: an error recorded after the exchange stays for the next query.
@@ -144,6 +145,8 @@ __global__ void status_take_kernel(uint32_t* status) {
   status[3] = code != 0u ? atomicExch(status + 1, 0u) : 0u;
 }
 
+// One CTA waits on a barrier that nothing completes; the bounded wait gives up
+// after limit_ns and the timeout is recorded.  Nothing is in flight.
 __global__ void expire_probe_kernel(uint32_t* status, uint64_t limit_ns) {
   __shared__ __align__(8) uint64_t bar;
   if (threadIdx.x == 0) {
@@ -160,13 +163,16 @@ __global__ void expire_probe_kernel(uint32_t* status, uint64_t limit_ns) {
 }  // namespace
 
 cudaError_t launch_guarded_kernel(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
-                                  const float* B, int64_t ldb, float* C, int64_t ldc, int scaled,
-                                  float alpha, float beta, cudaStream_t stream) {
+                                  bool trans_a, const float* B, int64_t ldb, bool trans_b,
+                                  float* C, int64_t ldc, int scaled, float alpha, float beta,
+                                  cudaStream_t stream) {
   const int64_t tiles_m = (M + kGBM - 1) / kGBM, tiles_n = (N + kGBN - 1) / kGBN;
   const int64_t tiles = tiles_m * tiles_n;
   if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
-  guarded_kernel<<<unsigned(tiles), kGThreads, 0, stream>>>(M, N, K, A, lda, B, ldb, C, ldc,
-                                                            tiles_n, scaled, alpha, beta);
+  const int64_t a_m = trans_a ? 1 : lda, a_k = trans_a ? lda : 1;
+  const int64_t b_k = trans_b ? 1 : ldb, b_n = trans_b ? ldb : 1;
+  guarded_kernel<<<unsigned(tiles), kGThreads, 0, stream>>>(M, N, K, A, a_m, a_k, B, b_k, b_n, C,
+                                                            ldc, tiles_n, scaled, alpha, beta);
   return cudaGetLastError();
 }
 

@@ -80,9 +80,12 @@ struct SmallShape {
 SmallShape small_shape();
 cudaError_t launch_small_kernel(const SmallArgs& args, int64_t tiles, cudaStream_t stream);
 
+// trans_a: A holds op(A)^T (K x M, row stride lda); trans_b: B holds op(B)^T
+// (N x K, row stride ldb).  Any alignment and stride.
 cudaError_t launch_guarded_kernel(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
-                                  const float* B, int64_t ldb, float* C, int64_t ldc, int scaled,
-                                  float alpha, float beta, cudaStream_t stream);
+                                  bool trans_a, const float* B, int64_t ldb, bool trans_b,
+                                  float* C, int64_t ldc, int scaled, float alpha, float beta,
+                                  cudaStream_t stream);
 
 // dst (rows x cols, row stride ld_dst, 16-byte aligned, ld_dst a multiple of
 // 4) = src (any row stride and alignment).  Columns cols..ld_dst-1 of dst are

@@ -117,6 +117,10 @@ struct GemmArgs {
   // access to C is then a 4-byte one (in the general epilogue, which also
   // applies alpha and beta: alpha = 1, beta = 0 leave acc unchanged).
   int32_t c_scalar;
+  // Nonzero when A arrives M-major (the operand is A^T stored K x M, M
+  // fastest): tmap_a then has box {BM, BK} and its copies land in the A ring
+  // as the compute warps read it, with no staging and no transposition.
+  int32_t a_mn;
 };
 
 // Tile configurations of the pipelined kernel (compiled instances, by id).
@@ -138,7 +142,8 @@ TileShape tile_shape(TileConfig cfg);
 int tile_kernel_prepare(TileConfig cfg);
 
 // tmap_a: A as a 2-D tensor (K fastest) with box {16, a_box_rows} and the
-// 64-byte swizzle; tmap_b: B (N fastest) with box {BN, 16}, no swizzle.
+// 64-byte swizzle, or, when args.a_mn, A^T's storage (M fastest) with box
+// {BM, 16} and no swizzle; tmap_b: B (N fastest) with box {BN, 16}, no swizzle.
 cudaError_t launch_tile_kernel(TileConfig cfg, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                                const GemmArgs& args, const Sched& sched, int grid,
                                cudaStream_t stream);

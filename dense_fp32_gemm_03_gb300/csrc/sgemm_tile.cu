@@ -46,8 +46,44 @@
 #include "sgemm_device.cuh"
 #include "sgemm_plan.h"
 #include "sgemm_sched.cuh"
+#include "sgemm_trace.h"
 
 namespace gb300 {
+
+#ifdef SGEMM_PHASE_TRACE
+__device__ uint64_t* g_trace_buf;
+__device__ int64_t g_trace_ctas;
+
+// Phase records of one CTA (one writing thread per log).
+struct TraceLog {
+  uint64_t* rec;
+  int n, end;
+  __device__ __forceinline__ void init(int first, int last) {
+    rec = int64_t(blockIdx.x) < g_trace_ctas ? g_trace_buf + size_t(blockIdx.x) * kTraceSlots * 2
+                                             : nullptr;
+    n = first;
+    end = last;
+  }
+  __device__ __forceinline__ void put(uint32_t kind, uint32_t a, uint32_t b) {
+    if (rec == nullptr || n >= end) return;
+    rec[2 * n] = dev::global_timer_ns();
+    rec[2 * n + 1] = (uint64_t(kind) << 56) | (uint64_t(a & 0xffffffu) << 32) | b;
+    ++n;
+  }
+  __device__ __forceinline__ void entry() {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    put(kTrEntry, smid, 0);
+  }
+};
+#else
+struct TraceLog {
+  __device__ __forceinline__ void init(int, int) {}
+  __device__ __forceinline__ void put(uint32_t, uint32_t, uint32_t) {}
+  __device__ __forceinline__ void entry() {}
+};
+#endif
+
 namespace {
 
 constexpr uint32_t kStatusTimeout = 3;  // SGEMM_ERR_TIMEOUT
@@ -172,6 +208,13 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
   const int lane = tid & 31, warp = tid >> 5;
   const int cta = blockIdx.x, ctas = gridDim.x;
   const uint64_t limit = args.wait_limit_ns;
+  TraceLog trace;
+  if (tid == 0) {
+    trace.init(0, kTraceProducerSlot0);
+    trace.entry();
+  } else if (tid == T::kConsumers) {
+    trace.init(kTraceProducerSlot0, kTraceSlots);
+  }
 
   if (tid == 0) {
     for (int s = 0; s < T::S; ++s) {
@@ -203,6 +246,31 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
       dev::tma_prefetch_desc(&tmap_a);
       if (pw == 0) dev::tma_prefetch_desc(&tmap_b);
     }
+    if (args.a_mn) {
+      // A^T's storage is M-major: one copy of the BK x BM tile lands in the
+      // ring exactly as the compute warps read it ([k][m]).  One lane issues
+      // both tiles of a stage; every producer thread arrives on full[s].
+      KCursor cur;
+      cur.init(sc, cta, ctas);
+      uint32_t i = 0;
+      for (; cur.valid; ++i) {
+        const uint32_t s = i % T::S, n = i / T::S;
+        if (n > 0 && !dev::mbar_wait_abortable(&empty[s], (n - 1) & 1u, limit, s_abort))
+          fail(kWaitTileStage);
+        if (pw == 0 && lane == 0 && !*s_abort) {
+          dev::mbar_expect_tx(&full[s], T::kBStageBytes + T::kAStageFloats * 4);
+          const int k0 = (cur.u.kb + cur.j) * T::BK;
+          dev::tma_load_2d(sB + s * T::kBStageFloats, &tmap_b, cur.tn * T::BN, k0, &full[s]);
+          dev::tma_load_2d(sA + s * T::kAStageFloats, &tmap_a, cur.tm * T::BM, k0, &full[s]);
+        }
+        dev::mbar_arrive(&full[s]);
+        cur.advance(sc, ctas);
+      }
+      if (*s_abort && pw == 0 && lane == 0)
+        for (uint32_t k = (i > T::S ? i - T::S : 0); k < i; ++k)
+          dev::mbar_wait(&full[k % T::S], (k / T::S) & 1u, limit);
+      return;
+    }
     KCursor issue, proc;
     issue.init(sc, cta, ctas);
     proc.init(sc, cta, ctas);
@@ -232,6 +300,7 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
       issue.advance(sc, ctas);
     }
     const uint32_t b_issued = issued;
+    if (pw == 0 && lane == 0) trace.put(kTrProducerIssued, 0, 0);
     uint32_t i = 0;
     for (; proc.valid; ++i) {
       const uint32_t s = i % T::S, n = i / T::S;
@@ -312,6 +381,7 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
     for (int j = 0; j < nk; ++j, ++it) {
       const uint32_t s = it % T::S;
       if (!dev::mbar_wait_abortable(&full[s], (it / T::S) & 1u, limit, s_abort)) fail(kWaitTileStage);
+      if (it == 0 && tid == 0) trace.put(kTrFirstStage, 0, 0);
       const float* a_buf = sA + s * T::kAStageFloats + a_frag;
       const float* b_buf = sB + s * T::kBStageFloats + b_frag;
       struct Frag {
@@ -367,6 +437,7 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
       if (lane == 0) dev::mbar_arrive(&empty[s]);
     }
 
+    if (tid == 0) trace.put(kTrKLoopEnd, uint32_t(u.tile), uint32_t(nk));
     // ---- epilogue
     // Thread value j is the float4 of patch row r = j / Q, column quad h = j % Q.
     constexpr int Q = T::kTN / 4;
@@ -427,6 +498,7 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
 #pragma unroll
         for (int j = 0; j < T::kOutVec; ++j) store_c(j, value(j));
       }
+      if (tid == 0) trace.put(kTrStoreEnd, uint32_t(u.tile), 0);
       continue;
     }
 
@@ -463,6 +535,7 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
       dev::named_barrier(1, T::kConsumers);
       last = *s_last != 0;
       dev::named_barrier(1, T::kConsumers);  // s_last may be rewritten by the next split tile
+      if (tid == 0) trace.put(kTrPublishEnd, uint32_t(u.tile), 0);
     }
     if (last) {
       // Every other partial is in the workspace.
@@ -513,9 +586,13 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
 #pragma unroll
         for (int j = 0; j < T::kOutVec; ++j) store_c(j, sum[j]);
       }
-      if (tid == 0) args.counters[u.t_sk] = 0;
+      if (tid == 0) {
+        args.counters[u.t_sk] = 0;
+        trace.put(kTrReduceEnd, uint32_t(u.tile), uint32_t(others));
+      }
     }
   }
+  if (tid == 0) trace.put(kTrExit, 0, 0);
 }
 
 template <class T>
@@ -635,3 +712,15 @@ cudaError_t launch_tile_kernel(TileConfig cfg, const CUtensorMap& tmap_a, const 
 }
 
 }  // namespace gb300
+
+#ifdef SGEMM_PHASE_TRACE
+extern "C" __attribute__((visibility("default"))) int sgemm_trace_configure(void* device_buffer,
+                                                                           int64_t ctas) {
+  uint64_t* buf = static_cast<uint64_t*>(device_buffer);
+  if (buf == nullptr) ctas = 0;
+  if (cudaMemcpyToSymbol(gb300::g_trace_buf, &buf, sizeof(buf)) != cudaSuccess ||
+      cudaMemcpyToSymbol(gb300::g_trace_ctas, &ctas, sizeof(ctas)) != cudaSuccess)
+    return 1;
+  return 0;
+}
+#endif

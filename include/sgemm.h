@@ -118,6 +118,40 @@ sgemm_status_t sgemm_ex(int layout, int64_t M, int64_t N, int64_t K, float alpha
                         int64_t lda, const float *B, int64_t ldb, float beta, float *C,
                         int64_t ldc, cudaStream_t stream);
 
+/* Transposition of one operand of sgemm_ex2(). */
+typedef enum {
+  SGEMM_OP_N = 0, /* op(X) = X */
+  SGEMM_OP_T = 1  /* op(X) = X^T */
+} sgemm_op_t;
+
+/*
+ * C = alpha * op(A) * op(B) + beta * C with a transposition flag per operand
+ * (each an sgemm_op_t): the general form of sgemm_ex(), with the alpha/beta
+ * epilogue the pages print ("Vectorized Memory Access ...", section 5;
+ * "2D Block Tiling ...", section 5) and the transposed / column-major operand
+ * layouts of "cuSgemm" (Kernel 7 takes column-major operands).  op(A) is
+ * M x K and op(B) is K x N.  The memory holds the stored matrices: A is M x K
+ * when trans_a == SGEMM_OP_N and K x M when SGEMM_OP_T (op(A) = A^T); B is
+ * K x N or N x K likewise.  `layout` applies to the stored A, B and C; the
+ * leading dimensions are the stored matrices' (row strides for
+ * SGEMM_ROW_MAJOR, column strides for SGEMM_COL_MAJOR), so for instance a
+ * row-major A with trans_a == SGEMM_OP_T needs lda >= M.
+ *
+ * How each operand reaches the kernels (row-major view; a column-major
+ * problem runs as the row-major C^T = op(B)^T op(A)^T over the same memory):
+ * a transposed A is read in place by the pipelined kernels as an M-major
+ * tile (TMA, no copy) when it is 16-byte aligned with lda a multiple of 4,
+ * and otherwise (or for the small-product kernel) transposed into the
+ * workspace first; a transposed B is always transposed into the workspace
+ * first (about 8 bytes of HBM traffic per element and one extra launch).
+ * sgemm_ex2 with two SGEMM_OP_N flags is sgemm_ex().  Errors, workspace and
+ * C semantics as for sgemm_ex(); a flag other than SGEMM_OP_N or SGEMM_OP_T
+ * returns SGEMM_ERR_INVALID_VALUE.
+ */
+sgemm_status_t sgemm_ex2(int layout, int trans_a, int trans_b, int64_t M, int64_t N, int64_t K,
+                         float alpha, const float *A, int64_t lda, const float *B, int64_t ldb,
+                         float beta, float *C, int64_t ldc, cudaStream_t stream);
+
 /*
  * As sgemm() but forces `variant` (an sgemm_variant_t).  The four pipelined
  * variants (TILED, STREAMK, TILED_SMALL, STREAMK_SMALL) and SMALL given operands they

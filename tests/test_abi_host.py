@@ -106,3 +106,30 @@ def test_null_pointers_allowed_for_empty_extents(lib):
     """M == 0 or N == 0 is a no-op; K == 0 needs only C.  Validation accepts them
     (they then need a device, so only the validator is exercised here)."""
     assert lib.sgemm_workspace_size(binding.STREAMK, 0, 4, 4) == 0
+
+
+@pytest.mark.parametrize("args", [
+    (0, 2, 0, 4, 4, 4),       # trans_a neither N nor T
+    (0, 0, -1, 4, 4, 4),      # trans_b neither N nor T
+    (5, 0, 0, 4, 4, 4),       # unknown layout
+])
+def test_ex2_rejects_bad_flags(lib, args):
+    layout, ta, tb, M, N, K = args
+    assert lib.sgemm_ex2(layout, ta, tb, M, N, K, 1.0, P_A, 8, P_B, 8, 0.0, P_C, 8, None) == \
+        binding.ERR_INVALID_VALUE
+
+
+@pytest.mark.parametrize("args", [
+    # (trans_a, trans_b, M, N, K, lda, ldb, ldc): leading dimensions of the stored matrices
+    (1, 0, 8, 4, 3, 7, 4, 4),     # A stored K x M needs lda >= M = 8
+    (0, 1, 4, 8, 3, 3, 2, 8),     # B stored N x K needs ldb >= K = 3
+    (1, 1, 5, 6, 9, 5, 8, 6),     # both transposed: ldb >= K = 9 fails
+])
+def test_ex2_checks_stored_leading_dimensions(lib, args):
+    ta, tb, M, N, K, lda, ldb, ldc = args
+    assert lib.sgemm_ex2(0, ta, tb, M, N, K, 1.0, P_A, lda, P_B, ldb, 0.0, P_C, ldc, None) == \
+        binding.ERR_INVALID_VALUE
+    # The same leading dimensions are fine once they cover the stored rows.
+    st = lib.sgemm_ex2(0, ta, tb, M, N, K, 1.0, P_A, max(lda, M if ta else K), P_B,
+                       max(ldb, K if tb else N), 0.0, P_C, ldc, None)
+    assert st != binding.ERR_INVALID_VALUE   # no device here: UNSUPPORTED
