@@ -465,7 +465,7 @@ int select_variant(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
   if (c_ok && (a_ok || trans_a) && (b_ok || trans_b)) {
     Plan p;
     const OpMode am = a_mode(fast, trans_a, a_ok);
-    if (!is_copy(am) && !trans_b && make_plan(fast, M, N, K, ds, &p) &&
+    if (am == kInPlace && !trans_b && make_plan(fast, M, N, K, ds, &p) &&
         find_specialized(p, M, N, K, ds) >= 0)
       return SGEMM_VARIANT_SPECIALIZED;
     return fast;
@@ -592,7 +592,8 @@ sgemm_status_t run(int variant, int64_t M, int64_t N, int64_t K, float alpha, co
   int spec = -1;
   if (specialized) {
     spec = find_specialized(p, M, N, K, *ds);
-    if (spec < 0 || is_copy(am) || is_copy(bm)) return SGEMM_ERR_UNSUPPORTED;
+    // The compiled-in instances read A K-major in place and B in place.
+    if (spec < 0 || am != kInPlace || bm != kInPlace) return SGEMM_ERR_UNSUPPORTED;
     if (scaled) spec = -1;
   }
   const TileShape ts = gb300::tile_shape(p.cfg);

@@ -153,6 +153,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// Copies `bytes` (a multiple of 16; both addresses 16-byte aligned) from
+// global memory to shared memory with the bulk copy engine, completing
+// `bytes` of transaction on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
 // ------------------------------------------------------------ FP32 arithmetic
 // d = a * b + d on both halves of a float pair, each with one IEEE rounding
 // (round to nearest even): two FP32 FFMAs issued as one instruction.

@@ -64,32 +64,44 @@ struct TraceLog {
     n = first;
     end = last;
   }
-  __device__ __forceinline__ void put(uint32_t kind, uint32_t a, uint32_t b) {
+  // The time is read before anything that waits for the log's pointer
+  // (whose load misses in L2 right after a flush).
+  __device__ __forceinline__ void put_at(uint64_t t, uint32_t kind, uint32_t a, uint32_t b) {
     if (rec == nullptr || n >= end) return;
-    rec[2 * n] = dev::global_timer_ns();
+    rec[2 * n] = t;
     rec[2 * n + 1] = (uint64_t(kind) << 56) | (uint64_t(a & 0xffffffu) << 32) | b;
     ++n;
   }
-  __device__ __forceinline__ void entry() {
+  __device__ __forceinline__ void put(uint32_t kind, uint32_t a, uint32_t b) {
+    put_at(dev::global_timer_ns(), kind, a, b);
+  }
+  __device__ __forceinline__ void entry(uint64_t t) {
     uint32_t smid;
     asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-    put(kTrEntry, smid, 0);
+    put_at(t, kTrEntry, smid, 0);
   }
+  static __device__ __forceinline__ uint64_t now() { return dev::global_timer_ns(); }
 };
 #else
 struct TraceLog {
   __device__ __forceinline__ void init(int, int) {}
   __device__ __forceinline__ void put(uint32_t, uint32_t, uint32_t) {}
-  __device__ __forceinline__ void entry() {}
+  __device__ __forceinline__ void put_at(uint64_t, uint32_t, uint32_t, uint32_t) {}
+  __device__ __forceinline__ void entry(uint64_t) {}
+  static __device__ __forceinline__ uint64_t now() { return 0; }
 };
 #endif
 
 namespace {
 
 constexpr uint32_t kStatusTimeout = 3;  // SGEMM_ERR_TIMEOUT
+// How long the CTA that owns a split tile's first k-tiles waits for the other
+// sharers' partial sums before publishing its own (see the split-tile epilogue).
+constexpr uint64_t kOwnerWaitNs = 5000;
+constexpr uint32_t kPfChunk = 16384;  // bytes per bulk copy of a prefetched partial tile
 
 template <int WARPS_M, int WARPS_N, int TN, int STAGES, int ASTAGES, bool DB, int CTAS,
-          int PRODUCER_REGS = 56, bool PAIRED_COLS = false>
+          int PRODUCER_REGS = 56, bool PAIRED_COLS = false, int PF_SLOTS = 0>
 struct TileCfg {
   static constexpr int kTR = 4, kTC = 8;    // lane grid of a consumer warp: rows x columns
   static constexpr int kTM = 8, kTN = TN;   // outputs per thread
@@ -130,12 +142,18 @@ struct TileCfg {
   static constexpr uint32_t kBStageBytes = kBStageFloats * 4;
   static constexpr uint32_t kAStagingBytes = kAStagingFloats * 4;
   static constexpr int kOutVec = kTM * kTN / 4;  // float4 values per thread
-  // Shared memory: [B ring][A staging: producer warp x slot][A ring][barriers][flags]
+  // Partial tiles of other CTAs that the producer prefetches into shared
+  // memory for the split tile this CTA finishes last (0: none).
+  static constexpr int kPfSlots = PF_SLOTS;
+  static constexpr uint32_t kSlotBytes = uint32_t(BM) * BN * 4;
+  // Shared memory: [B ring][A staging: producer warp x slot][A ring]
+  // [prefetched partials][barriers][flags]
   static constexpr size_t kBOff = 0;
   static constexpr size_t kAStagingOff = kBOff + size_t(S) * kBStageBytes;
   static constexpr size_t kAOff = kAStagingOff + size_t(kProducerWarps) * S2 * kAStagingBytes;
-  static constexpr size_t kBarOff = kAOff + size_t(S) * kAStageFloats * 4;
-  static constexpr size_t kFlagOff = kBarOff + size_t(2 * S + kProducerWarps * S2) * 8;
+  static constexpr size_t kPfOff = kAOff + size_t(S) * kAStageFloats * 4;
+  static constexpr size_t kBarOff = kPfOff + size_t(PF_SLOTS) * kSlotBytes;
+  static constexpr size_t kFlagOff = kBarOff + size_t(2 * S + kProducerWarps * S2 + 1) * 8;
   static constexpr size_t kSmem = kFlagOff + 16;
   static_assert(TN == 8 || TN == 16, "patch width");
   static_assert(ASTAGES <= STAGES, "the prologue's B tiles must fit the empty ring");
@@ -157,7 +175,7 @@ struct TileCfg {
 using Cfg0 = TileCfg<4, 2, 16, 6, 4, false, 1, 56, true>;   // 128 x 256 tile, 8 + 4 warps, 8x16 patch
 using Cfg1 = TileCfg<4, 2, 16, 6, 4, false, 1>;             // Cfg0, one-row quarter-warps
 using Cfg2 = TileCfg<4, 2, 16, 6, 4, true, 1, 56, true>;    // Cfg1 with fragment double buffering
-using Cfg3 = TileCfg<4, 2, 8, 4, 4, true, 1>;               // 128 x 128 tile, 8 + 4 warps, 8x8 patch
+using Cfg3 = TileCfg<4, 2, 8, 4, 4, true, 1, 56, false, 1>; // 128 x 128 tile, 8 + 4 warps, 8x8 patch
 using Cfg4 = TileCfg<4, 2, 8, 4, 4, true, 1, 56, true>;     // Cfg3, paired-column lane layout
 using Cfg5 = TileCfg<4, 2, 8, 4, 4, false, 1, 56, true>;    // Cfg4 without double buffering
 
@@ -183,10 +201,11 @@ auto with_cfg(int id, F&& f) {
 // shape and the Stream-K schedule of kSpecializedResident CTAs are compile-
 // time constants, so tile coordinates, shares and bounds fold into the code.
 // The launch must pass exactly that schedule (the host checks).
-template <class T, bool SCALED, int FM = 0, int FN = 0, int FK = 0>
+template <class T, bool SCALED, bool AMN = false, int FM = 0, int FN = 0, int FK = 0>
 __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
     tile_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                 const GemmArgs args, const Sched sc_in) {
+  const uint64_t t_entry = TraceLog::now();
   Sched sc = sc_in;
   if constexpr (FM > 0) {
     constexpr LaunchPlan kPlan =
@@ -201,20 +220,17 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + T::kBarOff);
   uint64_t* empty = full + T::S;
   uint64_t* astage = empty + T::S;  // [producer warp][slot]
+  uint64_t* pf_full = astage + T::kProducerWarps * T::S2;  // prefetched partials landed
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + T::kFlagOff);
   int* s_last = reinterpret_cast<int*>(smem + T::kFlagOff + 4);
+  volatile int* s_epi = reinterpret_cast<volatile int*>(smem + T::kFlagOff + 8);  // owner epilogue reached
+  volatile int* s_pf = reinterpret_cast<volatile int*>(smem + T::kFlagOff + 12);  // partials prefetched
 
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   const int cta = blockIdx.x, ctas = gridDim.x;
   const uint64_t limit = args.wait_limit_ns;
   TraceLog trace;
-  if (tid == 0) {
-    trace.init(0, kTraceProducerSlot0);
-    trace.entry();
-  } else if (tid == T::kConsumers) {
-    trace.init(kTraceProducerSlot0, kTraceSlots);
-  }
 
   if (tid == 0) {
     for (int s = 0; s < T::S; ++s) {
@@ -222,10 +238,19 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
       dev::mbar_init(&empty[s], T::kConsumerWarps);  // one arrival per consumer warp
     }
     for (int s = 0; s < T::kProducerWarps * T::S2; ++s) dev::mbar_init(&astage[s], 1);
+    dev::mbar_init(pf_full, 1);
     *s_abort = 0;
+    *s_epi = 0;
+    *s_pf = 0;
     dev::mbar_init_fence();
   }
   __syncthreads();
+  if (tid == 0) {
+    trace.init(0, kTraceProducerSlot0);
+    trace.entry(t_entry);
+  } else if (tid == T::kConsumers) {
+    trace.init(kTraceProducerSlot0, kTraceSlots);
+  }
 
   // A wait that failed: record it once, make every later wait of the CTA give
   // up at once, and carry on without waiting so that nothing hangs.
@@ -236,17 +261,92 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
     }
   };
 
+  // The CTAs that share split tile t_sk, [c_first, c_last] in CTA order.
+  auto sharers = [&](int t_sk, int& c_first, int& c_last) {
+    const int64_t first_iter = int64_t(t_sk) * sc.iters_per_tile;
+    c_first = sk_owner(sc, first_iter);
+    c_last = sk_owner(sc, first_iter + sc.iters_per_tile - 1);
+  };
+
+  // Prefetch of the other sharers' partial tiles for the split tile this CTA
+  // finishes last.  The CTA that owns a split tile's first k-tiles computes
+  // them at the end of its share, and the other sharers have usually
+  // published their partials by then; reading those from L2 after the last
+  // k-tile was most of the hand-off's cost.  Once every other sharer has
+  // arrived, producer warp 0 bulk-copies up to kPfSlots partials into shared
+  // memory while the compute warps finish.  It stops polling kOwnerWaitNs
+  // after the compute warps reached that epilogue (they then publish as
+  // usual); it always arrives on pf_full exactly once, with the number of
+  // partials copied in s_pf.
+  auto prefetch_partials = [&]() {
+    if constexpr (T::kPfSlots > 0) {
+      if (warp != T::kConsumerWarps || lane != 0) return;
+      WorkIter wl;
+      wl.init(sc, cta);
+      Unit lu{}, uu;
+      bool any = false;
+      while (wl.next(sc, ctas, uu)) {
+        lu = uu;
+        any = true;
+      }
+      if (!any || lu.t_sk < 0 || (lu.kb == 0 && lu.ke == sc.iters_per_tile)) return;
+      int c_first, c_last;
+      sharers(lu.t_sk, c_first, c_last);
+      const int others = c_last - c_first;
+      if (c_first != cta || others == 0) return;
+      int npf = 0;
+      if (!*s_abort) {
+        const int32_t* cnt = args.counters + lu.t_sk;
+        const uint64_t t0 = dev::global_timer_ns();
+        uint64_t t_epi = 0;
+        int seen = dev::ld_acquire_gpu(cnt);
+        while (seen != others && !*s_abort) {
+          const uint64_t t = dev::global_timer_ns();
+          if (*s_epi) {
+            if (t_epi == 0) t_epi = t;
+            else if (t - t_epi > kOwnerWaitNs) break;
+          }
+          if (t - t0 > limit) break;
+          __nanosleep(128);
+          seen = dev::ld_acquire_gpu(cnt);
+        }
+        if (seen == others) {
+          // The partials were written through the generic proxy; the bulk
+          // copies read them through the async proxy.
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          npf = others < T::kPfSlots ? others : T::kPfSlots;
+          *s_pf = npf;
+          dev::mbar_arrive_expect_tx(pf_full, uint32_t(npf) * T::kSlotBytes);
+          for (int i = 0; i < npf; ++i) {
+            const unsigned char* src = reinterpret_cast<const unsigned char*>(
+                args.partials + int64_t(lu.t_sk + c_first + 1 + i) * (int64_t(T::BM) * T::BN));
+            unsigned char* dst = smem + T::kPfOff + size_t(i) * T::kSlotBytes;
+            for (uint32_t off = 0; off < T::kSlotBytes; off += kPfChunk)
+              dev::bulk_load(dst + off, src + off, kPfChunk, pf_full);
+          }
+        }
+      }
+      if (npf == 0) {
+        *s_pf = 0;
+        dev::mbar_arrive(pf_full);
+      }
+      // The CTA must not exit with copies in flight.
+      if (!dev::mbar_wait(pf_full, 0, limit)) fail(kWaitTileStage);
+    }
+  };
+
   if (warp >= T::kConsumerWarps) {
     // ================================================ producer warpgroup
     if constexpr (T::kHandOver) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(T::kRegsProducer));
     const int pw = warp - T::kConsumerWarps;  // this warp owns A rows [32 pw, 32 pw + 32)
+    if (pw == 0 && lane == 0) trace.put(kTrProducerStart, 0, 0);
     uint64_t* my_astage = astage + pw * T::S2;
     float* my_staging = sAst + pw * T::S2 * T::kAStagingFloats;
     if (lane == 0) {
       dev::tma_prefetch_desc(&tmap_a);
       if (pw == 0) dev::tma_prefetch_desc(&tmap_b);
     }
-    if (args.a_mn) {
+    if constexpr (AMN) {
       // A^T's storage is M-major: one copy of the BK x BM tile lands in the
       // ring exactly as the compute warps read it ([k][m]).  One lane issues
       // both tiles of a stage; every producer thread arrives on full[s].
@@ -269,6 +369,7 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
       if (*s_abort && pw == 0 && lane == 0)
         for (uint32_t k = (i > T::S ? i - T::S : 0); k < i; ++k)
           dev::mbar_wait(&full[k % T::S], (k / T::S) & 1u, limit);
+      prefetch_partials();
       return;
     }
     KCursor issue, proc;
@@ -311,6 +412,7 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
         if (pw == 0 && lane == 0 && !*s_abort) issue_b(proc, s);
       }
       if (!dev::mbar_wait_abortable(&my_astage[s2], n2 & 1u, limit, s_abort)) fail(kWaitTileStage);
+      if (i == 0 && pw == 0 && lane == 0) trace.put(kTrFirstALanded, 0, 0);
       // Transpose this warp's 32 rows: staging [r][k] (64-byte swizzled rows:
       // 16-byte chunk q of row r sits at q ^ ((r >> 1) & 3)) -> ring [k][m].
       // Consecutive lanes write consecutive m: conflict-free 4-byte stores.
@@ -350,6 +452,7 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
         for (uint32_t k = (i > T::S ? i - T::S : 0); k < i; ++k)
           dev::mbar_wait(&full[k % T::S], (k / T::S) & 1u, limit);
     }
+    prefetch_partials();
     return;
   }
 
@@ -509,15 +612,46 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
     // last and publishes nothing; if it turns out last after publishing, it
     // still adds from its registers.  Either way the sum is the same
     // sequence of additions, so the result does not depend on who is last.
-    const int64_t t_first_iter = int64_t(u.t_sk) * sc.iters_per_tile;
-    const int c_first = sk_owner(sc, t_first_iter);
-    const int c_last = sk_owner(sc, t_first_iter + sc.iters_per_tile - 1);
+    int c_first, c_last;
+    sharers(u.t_sk, c_first, c_last);
     const int others = c_last - c_first;
     const int64_t tile_floats = int64_t(T::BM) * T::BN;
     const bool own_first = cta == c_first;
     bool last = false;
-    if (own_first) {
-      if (tid == 0) *s_last = dev::ld_acquire_gpu(args.counters + u.t_sk) == others ? 1 : 0;
+    int npf = 0;  // other sharers' partials already in shared memory
+    if constexpr (T::kPfSlots > 0) {
+      WorkIter wp = w;
+      Unit un;
+      if (own_first && others > 0 && !wp.next(sc, ctas, un)) {
+        // This CTA's last unit: the producer prefetches (or gives up on) the
+        // other sharers' partials and always arrives on pf_full.
+        if (tid == 0) *s_epi = 1;
+        if (!dev::mbar_wait_abortable(pf_full, 0, limit, s_abort)) fail(kWaitTileStage);
+        npf = *s_pf;
+        if (npf > 0) last = true;  // every other sharer had arrived
+        if (tid == 0) trace.put(kTrOwnerWait, uint32_t(u.tile), npf > 0 ? 2u : 0u);
+      }
+    }
+    if (own_first && !last) {
+      // The other sharers usually finish their parts at about the same time
+      // (a sharer whose whole share lies in this tile ends with it).  Waiting
+      // a little for their arrivals costs less than publishing this partial
+      // and reading it back, so poll the counter for up to kOwnerWaitNs; if
+      // they are not all in by then, publish as any sharer does.  The wait is
+      // bounded, so no CTA depends on another being resident.
+      if (tid == 0) {
+        const int32_t* cnt = args.counters + u.t_sk;
+        int seen = dev::ld_acquire_gpu(cnt);
+        if (seen != others) {
+          const uint64_t t0 = dev::global_timer_ns();
+          while (seen != others && dev::global_timer_ns() - t0 < kOwnerWaitNs) {
+            __nanosleep(64);
+            seen = dev::ld_acquire_gpu(cnt);
+          }
+        }
+        *s_last = seen == others ? 1 : 0;
+        trace.put(kTrOwnerWait, uint32_t(u.tile), seen == others ? 1u : 0u);
+      }
       dev::named_barrier(1, T::kConsumers);
       last = *s_last != 0;
       dev::named_barrier(1, T::kConsumers);  // s_last is rewritten below
@@ -535,7 +669,7 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
       dev::named_barrier(1, T::kConsumers);
       last = *s_last != 0;
       dev::named_barrier(1, T::kConsumers);  // s_last may be rewritten by the next split tile
-      if (tid == 0) trace.put(kTrPublishEnd, uint32_t(u.tile), 0);
+      if (tid == 0) trace.put(kTrPublishEnd, uint32_t(u.tile), last ? 1u : 0u);
     }
     if (last) {
       // Every other partial is in the workspace.
@@ -546,10 +680,18 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
         // acc += partial, CTA after CTA, with a slot's loads in flight at once.
 #pragma unroll 1
         for (int cc = c_first + 1; cc <= c_last; ++cc) {
-          const float4* src = base + (u.t_sk + cc) * slot_vec;
           float4 v[T::kOutVec];
+          if (cc - c_first - 1 < npf) {
+            const float4* src = reinterpret_cast<const float4*>(
+                                    smem + T::kPfOff + size_t(cc - c_first - 1) * T::kSlotBytes) +
+                                tid;
 #pragma unroll
-          for (int j = 0; j < T::kOutVec; ++j) v[j] = __ldcg(src + j * T::kConsumers);
+            for (int j = 0; j < T::kOutVec; ++j) v[j] = src[j * T::kConsumers];
+          } else {
+            const float4* src = base + (u.t_sk + cc) * slot_vec;
+#pragma unroll
+            for (int j = 0; j < T::kOutVec; ++j) v[j] = __ldcg(src + j * T::kConsumers);
+          }
 #pragma unroll
           for (int j = 0; j < T::kOutVec; ++j) {
             const int r = j / Q, h = j % Q;
@@ -600,6 +742,10 @@ int prepare() {
   if (cudaFuncSetAttribute(tile_kernel<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(T::kSmem)) != cudaSuccess ||
       cudaFuncSetAttribute(tile_kernel<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(T::kSmem)) != cudaSuccess ||
+      cudaFuncSetAttribute(tile_kernel<T, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(T::kSmem)) != cudaSuccess ||
+      cudaFuncSetAttribute(tile_kernel<T, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(T::kSmem)) != cudaSuccess)
     return -1;
   int blocks = 0;
@@ -629,13 +775,13 @@ struct SpecInst {
   using T = typename CfgById<ID>::type;
   static SpecShape shape() { return SpecShape{ID, M, N, K}; }
   static bool prepare() {
-    return cudaFuncSetAttribute(tile_kernel<T, false, M, N, K>,
+    return cudaFuncSetAttribute(tile_kernel<T, false, false, M, N, K>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 int(T::kSmem)) == cudaSuccess;
   }
   static void launch(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const GemmArgs& args,
                      const Sched& sched, int grid, cudaStream_t stream) {
-    tile_kernel<T, false, M, N, K><<<grid, T::NT, T::kSmem, stream>>>(tmap_a, tmap_b, args, sched);
+    tile_kernel<T, false, false, M, N, K><<<grid, T::NT, T::kSmem, stream>>>(tmap_a, tmap_b, args, sched);
   }
 };
 
@@ -693,6 +839,7 @@ int specialized_prepare() { return spec_prepare_all(SpecIndex{}) ? 0 : -1; }
 cudaError_t launch_specialized(int i, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                                const GemmArgs& args, const Sched& sched, int grid,
                                cudaStream_t stream) {
+  if (args.a_mn || args.scaled || args.c_scalar) return cudaErrorInvalidValue;  // plain instances only
   if (!spec_launch_at(i, tmap_a, tmap_b, args, sched, grid, stream, SpecIndex{}))
     return cudaErrorInvalidValue;
   return cudaGetLastError();
@@ -703,10 +850,17 @@ cudaError_t launch_tile_kernel(TileConfig cfg, const CUtensorMap& tmap_a, const 
                                cudaStream_t stream) {
   return with_cfg(cfg, [&](auto c) {
     using T = decltype(c);
-    if (args.scaled || args.c_scalar)
+    const bool scaled = args.scaled || args.c_scalar;
+    if (args.a_mn) {
+      if (scaled)
+        tile_kernel<T, true, true><<<grid, T::NT, T::kSmem, stream>>>(tmap_a, tmap_b, args, sched);
+      else
+        tile_kernel<T, false, true><<<grid, T::NT, T::kSmem, stream>>>(tmap_a, tmap_b, args, sched);
+    } else if (scaled) {
       tile_kernel<T, true><<<grid, T::NT, T::kSmem, stream>>>(tmap_a, tmap_b, args, sched);
-    else
+    } else {
       tile_kernel<T, false><<<grid, T::NT, T::kSmem, stream>>>(tmap_a, tmap_b, args, sched);
+    }
     return cudaGetLastError();
   });
 }

@@ -21,10 +21,14 @@ enum TraceKind : uint32_t {
   kTrFirstStage = 2,     // the first ring stage has landed
   kTrKLoopEnd = 3,       // last k-tile of a unit computed       a = tile, b = k-tiles
   kTrStoreEnd = 4,       // whole tile stored to C               a = tile
-  kTrPublishEnd = 5,     // split tile's partial published       a = tile
+  kTrPublishEnd = 5,     // split tile's partial published       a = tile, b = 1: then last
   kTrReduceEnd = 6,      // split tile reduced and stored        a = tile, b = partials read
   kTrExit = 7,           // consumer warps done
   kTrProducerIssued = 8, // producer: first copies issued
+  kTrOwnerWait = 9,      // owner of a split tile done waiting    a = tile, b = 1: all arrived,
+                         //                                       2: partials prefetched
+  kTrProducerStart = 10, // producer warpgroup running (registers handed over)
+  kTrFirstALanded = 11,  // producer: its first A slice is in shared memory
 };
 
 constexpr int kTraceSlots = 64;
