@@ -321,16 +321,9 @@ bool make_plan(int variant, int64_t M, int64_t N, int64_t K, const DeviceState& 
 // The size-specialized instance compiled for exactly this planned launch, or -1.
 int find_specialized(const Plan& p, int64_t M, int64_t N, int64_t K, const DeviceState& ds) {
   if (p.variant != SGEMM_VARIANT_STREAMK && p.variant != SGEMM_VARIANT_STREAMK_SMALL) return -1;
-  if (int64_t(ds.sms) * ds.ctas_per_sm[p.cfg] != gb300::kSpecializedResident) return -1;
-  for (int i = 0; i < gb300::specialized_count(); ++i) {
-    const gb300::SpecShape s = gb300::specialized_shape(i);
-    if (s.cfg != p.cfg || s.m != M || s.n != N || s.k != K) continue;
-    const TileShape ts = gb300::tile_shape(p.cfg);
-    const gb300::LaunchPlan lp =
-        gb300::plan_launch(M, N, K, ts.bm, ts.bn, ts.bk, gb300::kSpecializedResident, true);
-    if (lp.ok && gb300::same_sched(lp.sc, p.sc) && lp.grid == p.grid) return i;
-  }
-  return -1;
+  const TileShape ts = gb300::tile_shape(p.cfg);
+  return gb300::find_specialized_plan(p.cfg, M, N, K, ts.bm, ts.bn, ts.bk,
+                                      int64_t(ds.sms) * ds.ctas_per_sm[p.cfg], p.sc, p.grid);
 }
 
 // Estimated duration (microseconds) of a planned fast variant on this device.

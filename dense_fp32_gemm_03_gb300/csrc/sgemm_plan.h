@@ -156,6 +156,32 @@ struct SpecShape {
   TileConfig cfg;
   int64_t m, n, k;
 };
+// The compiled instances, by index (the kernel translation unit checks that
+// its instance list matches this table).  768^3 and 1024^3 run 128 x 128
+// tiles (configuration 3), the larger sizes 128 x 256 (configuration 0).
+constexpr SpecShape kSpecShapes[] = {{0, 4096, 4096, 4096}, {3, 1024, 1024, 1024},
+                                     {3, 768, 768, 768},    {0, 1536, 1536, 1536},
+                                     {0, 2048, 2048, 2048}};
+constexpr int kSpecShapeCount = int(sizeof(kSpecShapes) / sizeof(kSpecShapes[0]));
+
+// The instance compiled for exactly this launch -- configuration `cfg` with
+// BM x BN x BK tiles, the planned schedule `sc` over `grid` CTAs, `resident`
+// CTAs able to run at once -- or -1.  An instance's schedule is compiled for
+// kSpecializedResident CTAs, so on a device with another SM count (times
+// CTAs per SM) nothing matches and the generic kernel runs.
+constexpr int find_specialized_plan(TileConfig cfg, int64_t M, int64_t N,
+                                         int64_t K, int bm, int bn, int bk,
+                                         int64_t resident, const Sched& sc,
+                                         int64_t grid) {
+  if (resident != kSpecializedResident) return -1;
+  for (int i = 0; i < kSpecShapeCount; ++i) {
+    const SpecShape& s = kSpecShapes[i];
+    if (s.cfg != cfg || s.m != M || s.n != N || s.k != K) continue;
+    const LaunchPlan lp = plan_launch(M, N, K, bm, bn, bk, kSpecializedResident, true);
+    if (lp.ok && same_sched(lp.sc, sc) && lp.grid == grid) return i;
+  }
+  return -1;
+}
 int specialized_count();
 SpecShape specialized_shape(int i);
 int specialized_prepare();  // 0, or < 0 on error

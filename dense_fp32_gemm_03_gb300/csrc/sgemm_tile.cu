@@ -773,6 +773,8 @@ struct CfgById<3> {
 template <int ID, int M, int N, int K>
 struct SpecInst {
   using T = typename CfgById<ID>::type;
+  static constexpr int kId = ID;
+  static constexpr int64_t kM = M, kN = N, kK = K;
   static SpecShape shape() { return SpecShape{ID, M, N, K}; }
   static bool prepare() {
     return cudaFuncSetAttribute(tile_kernel<T, false, false, M, N, K>,
@@ -789,6 +791,17 @@ using SpecList = std::tuple<SpecInst<0, 4096, 4096, 4096>, SpecInst<3, 1024, 102
                             SpecInst<3, 768, 768, 768>, SpecInst<0, 1536, 1536, 1536>,
                             SpecInst<0, 2048, 2048, 2048>>;
 constexpr int kSpecCount = int(std::tuple_size<SpecList>::value);
+static_assert(kSpecCount == kSpecShapeCount, "SpecList and kSpecShapes list the same instances");
+template <size_t... I>
+constexpr bool spec_table_matches(std::index_sequence<I...>) {
+  return ((kSpecShapes[I].cfg == std::tuple_element_t<I, SpecList>::kId &&
+           kSpecShapes[I].m == std::tuple_element_t<I, SpecList>::kM &&
+           kSpecShapes[I].n == std::tuple_element_t<I, SpecList>::kN &&
+           kSpecShapes[I].k == std::tuple_element_t<I, SpecList>::kK) &&
+          ...);
+}
+static_assert(spec_table_matches(std::make_index_sequence<kSpecCount>{}),
+              "SpecList and kSpecShapes list the same instances in the same order");
 using SpecIndex = std::make_index_sequence<std::tuple_size<SpecList>::value>;
 
 template <size_t... I>

@@ -17,35 +17,18 @@ decomposition's contract independently:
 """
 from __future__ import annotations
 
-import os
-import shutil
-import subprocess
-
 import pytest
 
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-CSRC = os.path.join(ROOT, "dense_fp32_gemm_03_gb300", "csrc")
-K_MIN_SK_ITERS = 4  # kMinSkIters in sgemm_plan.h: shorter shares are not worth splitting
+import plan_util
 
-FIELDS = ("ok", "tiles_m", "tiles_n", "ipt", "dp_tiles", "sk_tiles", "sk_ctas", "sk_base",
-          "sk_extra", "grid", "slots", "group_m")
+K_MIN_SK_ITERS = 4  # kMinSkIters in sgemm_plan.h: shorter shares are not worth splitting
 
 
 @pytest.fixture(scope="module")
-def probe(tmp_path_factory):
-    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
-    if shutil.which("g++") is None or not os.path.exists(os.path.join(cuda_inc, "cuda.h")):
+def probe():
+    if not plan_util.available():
         pytest.skip("needs g++ and the CUDA headers")
-    exe = str(tmp_path_factory.mktemp("plan") / "plan_probe")
-    subprocess.run(["g++", "-std=c++17", "-O1", "-I", CSRC, "-I", cuda_inc,
-                    os.path.join(ROOT, "tests", "plan_probe.cpp"), "-o", exe], check=True)
-
-    def plans(cases):
-        text = "".join(f"{M} {N} {K} {bm} {bn} {bk} {res} {int(sk)}\n"
-                       for M, N, K, bm, bn, bk, res, sk in cases)
-        out = subprocess.run([exe], input=text, capture_output=True, text=True, check=True).stdout
-        return [dict(zip(FIELDS, map(int, line.split()))) for line in out.splitlines()]
-    return plans
+    return plan_util.plans
 
 
 def ceil_div(a, b):
@@ -142,3 +125,28 @@ def test_split_tiles_have_distinct_slots(probe):
                 assert slot < p["slots"], (case, t, c)
                 assert slot not in used, (case, t, c)
                 used.add(slot)
+
+
+# The size-specialized instances (kSpecShapes in sgemm_plan.h): shape and tile.
+SPECIALIZED = [((4096, 4096, 4096), (128, 256)), ((1024, 1024, 1024), (128, 128)),
+               ((768, 768, 768), (128, 128)), ((1536, 1536, 1536), (128, 256)),
+               ((2048, 2048, 2048), (128, 256))]
+
+
+def test_specialized_instance_needs_the_compiled_sm_count(probe):
+    """The selector takes a size-specialized instance only when the device runs exactly the
+    152 CTAs its schedule was compiled for; any other SM count x CTAs per SM falls back."""
+    cs = [(M, N, K, bm, bn, 16, res, True)
+          for (M, N, K), (bm, bn) in SPECIALIZED for res in (152, 148, 144, 160, 304, 76, 1)]
+    for case, p in zip(cs, probe(cs)):
+        M, N, K, bm, bn, bk, res, sk = case
+        want = [s for s, _ in SPECIALIZED].index((M, N, K)) if res == 152 else -1
+        assert p["spec"] == want, case
+
+
+def test_specialized_instance_only_for_its_shape_and_tile(probe):
+    cs = [(4096, 4096, 4092, 128, 256, 16, 152, True), (1024, 1024, 2048, 128, 128, 16, 152, True),
+          (1024, 1024, 1024, 128, 256, 16, 152, True), (4096, 4096, 4096, 128, 128, 16, 152, True),
+          (2048, 2048, 2048, 128, 256, 16, 152, False), (1023, 1024, 1024, 128, 128, 16, 152, True)]
+    for case, p in zip(cs, probe(cs)):
+        assert p["spec"] == -1, case

@@ -1,0 +1,104 @@
+"""Full-size parity where the Stream-K schedule splits tiles over CTAs.
+
+Split tiles are where CTAs hand partial sums to each other, so they are
+compared element by element at the configurations' full sizes:
+
+* 1024 x 1024 x 16384 (long K): every tile is split, so the whole product is
+  compared, through the selector, Stream-K on 128 x 256 tiles and Stream-K on
+  128 x 128 tiles;
+* 16384 x 1024 x 4096 (tall), 8192^3 and 4096^3: whole tile-row blocks that hold
+  split tiles.  The blocks are chosen from the schedule itself (plan_launch,
+  read through tests/plan_probe.cpp): the test asserts that each block
+  contains split tiles of the variant it runs.
+
+Stream-K results are not bit-reproducible across schedules ("Beyond Kernel 7",
+"What the result establishes"), so the check is the FP32 bound per element
+and the pages' max|err|/max|ref| gate, not equality with another variant.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import dense_fp32_gemm_03_gb300 as sg
+from dense_fp32_gemm_03_gb300 import workloads
+
+import plan_util
+from parity import check_within_bound
+
+pytestmark = pytest.mark.gpu
+
+TILE = {sg.STREAMK: (128, 256), sg.STREAMK_SMALL: (128, 128), sg.SPECIALIZED: None}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    if not plan_util.available():
+        pytest.skip("needs g++ and the CUDA headers for the schedule probe")
+    import __graft_entry__
+    __graft_entry__.build()
+    yield
+    st, site = sg.query_device_status()
+    assert st == 0, f"device status {st} (site {site}) left after the module"
+
+
+def _resident():
+    # The tile kernels run one CTA per SM.
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def _tile_of(variant, A, B, C):
+    """(BM, BN) of the 16-deep tiles the variant runs for these operands."""
+    if variant == sg.AUTO:
+        variant = sg.select_variant(A, B, C)
+    if variant == sg.SPECIALIZED:
+        return None
+    return TILE[variant]
+
+
+def test_long_k_every_tile_split_full_compare():
+    w = workloads.LONG_K
+    A_h, B_h = workloads.operands(w)
+    ref, E = oracle.sgemm_f64(A_h, B_h)
+    A, B = A_h.cuda(), B_h.cuda()
+    C = torch.empty(w.M, w.N, device="cuda")
+    for v in (sg.AUTO, sg.STREAMK, sg.STREAMK_SMALL):
+        tile = _tile_of(v, A, B, C)
+        assert tile is not None
+        p = plan_util.plan(w.M, w.N, w.K, tile[0], tile[1], 16, _resident())
+        assert p["dp_tiles"] == 0 and p["sk_tiles"] == p["tiles_m"] * p["tiles_n"], p
+        C.fill_(float("nan"))
+        sg.sgemm(A, B, out=C, variant=v)
+        torch.cuda.synchronize()
+        check_within_bound(C.cpu().numpy(), ref, E, w.K, f"{w.name} variant {v} (full)")
+
+
+@pytest.mark.parametrize("w", [workloads.TALL, workloads.SQUARE_8192, workloads.SQUARE_4096],
+                         ids=lambda w: w.name)
+@pytest.mark.parametrize("variant", [sg.AUTO, sg.STREAMK], ids=["auto", "streamk"])
+def test_row_blocks_with_split_tiles(w, variant):
+    A_h, B_h = workloads.operands(w)
+    A, B = A_h.cuda(), B_h.cuda()
+    C = torch.full((w.M, w.N), float("nan"), device="cuda")
+    tile = _tile_of(variant, A, B, C)
+    assert tile is not None
+    bm, bn = tile
+    p = plan_util.plan(w.M, w.N, w.K, bm, bn, 16, _resident())
+    split = list(plan_util.split_tiles(p))
+    assert split, f"{w.name}: the schedule splits no tile"
+    # The tile rows of the first and the last split tile.
+    rows_of_split = sorted({plan_util.tile_coords(p, t)[0] for t in split})
+    blocks = sorted({rows_of_split[0], rows_of_split[-1]})
+    sg.sgemm(A, B, out=C, variant=variant)
+    torch.cuda.synchronize()
+    got = C.cpu().numpy()
+    assert np.all(np.isfinite(got)), f"{w.name}: tiles left unwritten"
+    for tm in blocks:
+        in_block = [t for t in split if plan_util.tile_coords(p, t)[0] == tm]
+        assert in_block, (w.name, tm)
+        rows = slice(tm * bm, min((tm + 1) * bm, w.M))
+        ref, E = oracle.sgemm_f64(A_h[rows], B_h)
+        check_within_bound(got[rows], ref, E, w.K,
+                           f"{w.name} variant {variant} tile row {tm} ({len(in_block)} split tiles)")
