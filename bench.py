@@ -58,6 +58,8 @@ def parse_args(argv=None):
                    help="one JSON line per workload of the configuration list (not the default line)")
     p.add_argument("--sweep-cpu-seconds", type=float, default=2.0,
                    help="host time of each oracle sample in --sweep (0: no oracle timing)")
+    p.add_argument("--out", default=None,
+                   help="--sweep: append each line to this file and skip workloads it already holds")
     return p.parse_args(argv)
 
 
@@ -211,6 +213,52 @@ def measured_traffic(workload: str):
     return float(traffic.group(1))
 
 
+# ------------------------------------------------------------ sweep checking
+U24 = 2.0 ** -24
+PAGES_GATE = 1e-4  # max|err| / max|ref| ("Beyond Kernel 7", "What the result establishes")
+
+
+def check_rows(C_rows, A_rows, B, K):
+    """The sweep's correctness figures for a block of rows of C against the oracle:
+    max relative error (over C_ref != 0), max|err| / max|ref| and whether every element
+    is within 4 K 2^-24 sum_k |a b| and the pages' gate holds."""
+    import numpy as np
+    import oracle
+    ref, E = oracle.sgemm_f64(A_rows, B)
+    got = np.asarray(C_rows, dtype=np.float64)
+    err = np.abs(got - ref)
+    nz = np.abs(ref) > 0
+    max_rel = float((err[nz] / np.abs(ref[nz])).max()) if np.any(nz) else 0.0
+    ref_max = float(np.abs(ref).max()) if ref.size else 0.0
+    norm = float(err.max()) / ref_max if ref_max > 0 else 0.0
+    ok = bool(np.all(np.isfinite(got)) and np.all(err <= 4.0 * K * U24 * E) and norm < PAGES_GATE)
+    return {"max_rel_err": max_rel, "max_err_over_max_ref": norm, "bound_ok": ok,
+            "rows_checked": int(got.shape[0])}
+
+
+def done_workloads(path):
+    """Workload names already in a sweep output file (missing file: none)."""
+    done = set()
+    try:
+        with open(path) as f:
+            for line in f:
+                try:
+                    rec = json.loads(line)
+                except ValueError:
+                    continue  # a line cut short by an interrupted run
+                if isinstance(rec, dict) and "workload" in rec:
+                    done.add(rec["workload"])
+    except OSError:
+        pass
+    return done
+
+
+def sweep_plan(workloads_all, out_path):
+    """The sweep's workloads that still need a line (resume: skip those in out_path)."""
+    done = done_workloads(out_path) if out_path else set()
+    return [w for w in workloads_all if w.dist != "int8range" and w.name not in done]
+
+
 def cpu_baseline(w, A, B, seconds: float, threads: int = 0):
     """Time the oracle (as it stands) on a bounded row sample of the workload, on all
     the host cores it may use (threads <= 0) or on `threads` of them."""
@@ -244,7 +292,7 @@ def _cpu_sample(w, A, B, seconds, oracle):
     return {"value": flops / dt2 / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"rows 0..{rows2 - 1} of the {w.M}x{w.N}x{w.K} product ({rows2}x{w.N} outputs, "
                       f"float64 triple loop{rep_note}, {total:.1f} s)",
-            "seconds": total}
+            "seconds": total, "rows": rows2}
 
 
 # ------------------------------------------------------------------------- arms
@@ -372,6 +420,36 @@ def e2e_pipelined(w, sg, device, variant, A_h, B_h, steps, warmup):
     return start.elapsed_time(end) / 1e3
 
 
+def e2e_per_call(w, sg, device, variant, A_h, B_h, calls, warmup):
+    """Per-call latency (microseconds) of one unpipelined end-to-end call on one stream:
+    host-to-device copies of A and B from pinned memory, the C-ABI multiply, and the
+    device-to-host copy of C, bracketed by CUDA events on that stream."""
+    import torch
+    A_pin, B_pin = A_h.pin_memory(), B_h.pin_memory()
+    A = torch.empty_like(A_pin, device=device)
+    B = torch.empty_like(B_pin, device=device)
+    C = torch.empty((w.M, w.N), device=device)
+    C_pin = torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()
+    s = torch.cuda.Stream(device)
+    times = []
+    for i in range(warmup + calls):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            A.copy_(A_pin, non_blocking=True)
+            B.copy_(B_pin, non_blocking=True)
+            st = sg.sgemm_raw(w.M, w.N, w.K, A.data_ptr(), w.K, B.data_ptr(), w.N, C.data_ptr(),
+                              w.N, s.cuda_stream, variant)
+            if st != 0:
+                raise RuntimeError(sg.status_string(st))
+            C_pin.copy_(C, non_blocking=True)
+            e1.record(s)
+        s.synchronize()
+        if i >= warmup:
+            times.append(e0.elapsed_time(e1) * 1e3)
+    return times
+
+
 def cublas_context(w, device, flush, steps=20):
     """torch.matmul with TF32 disabled (FP32 arithmetic) on the same inputs and protocol:
     a same-run context figure, as the pages compare against cuBLAS."""
@@ -456,10 +534,8 @@ def run_ours(args):
         flush_buf.fill_(1.0)
 
     if args.sweep:
-        for w in workloads.ALL:
-            if w.dist == "int8range":
-                continue
-            A_h, B_h, *_, times, chosen = bench_workload(w, args, sg, device, flush, variant)
+        for w in sweep_plan(workloads.ALL, args.out):
+            A_h, B_h, _, _, C, times, chosen = bench_workload(w, args, sg, device, flush, variant)
             ms = statistics.median(times)
             line = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
                     "variant": sg.variant_name(chosen), "us_median": ms * 1e3,
@@ -472,9 +548,23 @@ def run_ours(args):
                 cpu = {"all_cores": cpu_baseline(w, A_h, B_h, args.sweep_cpu_seconds)}
                 if max(w.M, w.N, w.K) <= 1024:
                     cpu["one_core"] = cpu_baseline(w, A_h, B_h, args.sweep_cpu_seconds, threads=1)
-                line["cpu_oracle"] = {k: {"tflops": v["value"], "cores": v["cores"], "sample": v["sample"]}
+                line["cpu_oracle"] = {k: {"tflops": v["value"], "cores": v["cores"], "sample": v["sample"],
+                                          "rows": v["rows"]}
                                       for k, v in cpu.items()}
-            print(json.dumps(line), flush=True)
+            if rank == 0:
+                # The result of the last timed call, checked against the oracle on the
+                # last rows of C (the grouped raster puts the Stream-K split tiles
+                # last): as many rows as the oracle's timing sample took, or about
+                # 2 GFLOP of oracle work when it did not run; at least 8.
+                rows = line.get("cpu_oracle", {}).get("all_cores", {}).get("rows") or 0
+                rows = max(8, min(w.M, rows or int(2e9 / (2.0 * w.N * w.K))))
+                C_h = C[w.M - rows:].cpu().numpy()
+                line.update(check_rows(C_h, A_h[w.M - rows:], B_h, w.K))
+            text = json.dumps(line)
+            print(text, flush=True)
+            if args.out and rank == 0:
+                with open(args.out, "a") as f:
+                    f.write(text + "\n")
         return 0
 
     w = workloads.BY_NAME[args.workload]
@@ -503,6 +593,9 @@ def run_ours(args):
     e2e_total = e2e_pipelined(w, sg, device, variant, A_h, B_h, e2e_steps, warmup=3)
     e2e_total = max_over_ranks(e2e_total, world, device)
     e2e_value = aggregate(w.flops * e2e_steps, e2e_total, world)
+    # The same call unpipelined: copy in, multiply, copy out, one call at a time.
+    lat = e2e_per_call(w, sg, device, variant, A_h, B_h, calls=max(3, min(args.steps, 20)), warmup=2)
+    lat_us = max_over_ranks(statistics.median(lat), world, device)
 
     # Secondary size (n = 1024) on the same device.
     w2 = workloads.SQUARE_1024
@@ -548,7 +641,10 @@ def run_ours(args):
                       "us_median": statistics.median(times2) * 1e3, "generic": generic2},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 4 * (w.M * w.K + w.K * w.N),
                 "d2h_bytes_per_step": 4 * w.M * w.N,
-                "pipelining": "copies of step i overlap the multiply of step i-1 (3 streams)"},
+                "pipelining": "copies of step i overlap the multiply of step i-1 (3 streams)",
+                "per_call": {"us_median": lat_us, "value": w.flops / (lat_us * 1e-6) / 1e12,
+                             "unit": UNIT, "calls": len(lat),
+                             "what": "one stream, no overlap: H2D of A and B, sgemm, D2H of C"}},
         "context": context,
         "tf32_mode": tf32,
         "gpu_launches": args.steps,
@@ -557,7 +653,7 @@ def run_ours(args):
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = {k: v for k, v in cpu_baseline(w, A_h, B_h, args.cpu_seconds).items()
-                                if k != "seconds"}
+                                if k not in ("seconds", "rows")}
     print(json.dumps(line), flush=True)
     return 0
 

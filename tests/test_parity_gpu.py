@@ -351,9 +351,13 @@ def test_graph_replay_after_workspace_regrowth():
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=s):
         sg.sgemm(A, B, out=C)
-    # A product whose split tiles need more workspace than 1024^3 left in the cache.
-    big = next(x for x in workloads.SWEEP if x.M == 1536)
-    assert sg.workspace_size(big.M, big.N, big.K) > 1.25 * sg.workspace_size(w.M, w.N, w.K)
+    # A product whose split tiles need more workspace than 1024^3 left in the cache
+    # (the cache holds 1.25 x what a call asked for).
+    need = 1.25 * sg.workspace_size(w.M, w.N, w.K)
+    big = next(x for x in (workloads.Workload(f"regrow_{m}x{n}x{k}", m, n, k, "normal", 1300 + m)
+                           for m, n, k in [(1536, 1536, 1536), (2048, 2048, 2048),
+                                           (2560, 2560, 1024), (4096, 4096, 512)])
+               if sg.workspace_size(x.M, x.N, x.K) > need)
     Ab, Bb = (x.cuda() for x in workloads.operands(big))
     with torch.cuda.stream(s):
         Cb = sg.sgemm(Ab, Bb)
