@@ -54,20 +54,23 @@ namespace gb300 {
 __device__ uint64_t* g_trace_buf;
 __device__ int64_t g_trace_ctas;
 
-// Phase records of one CTA (one writing thread per log).
+// Phase records of one CTA (one writing thread per log).  The log's pointer
+// and extent are loaded at set-up but first used by a record, and the times
+// are read before that, so that a record never waits on those loads (they
+// miss in L2 right after a flush) ahead of the phase it stamps.
 struct TraceLog {
-  uint64_t* rec;
+  uint64_t* buf;
+  int64_t cap;
   int n, end;
   __device__ __forceinline__ void init(int first, int last) {
-    rec = int64_t(blockIdx.x) < g_trace_ctas ? g_trace_buf + size_t(blockIdx.x) * kTraceSlots * 2
-                                             : nullptr;
+    buf = g_trace_buf;
+    cap = g_trace_ctas;
     n = first;
     end = last;
   }
-  // The time is read before anything that waits for the log's pointer
-  // (whose load misses in L2 right after a flush).
   __device__ __forceinline__ void put_at(uint64_t t, uint32_t kind, uint32_t a, uint32_t b) {
-    if (rec == nullptr || n >= end) return;
+    if (buf == nullptr || int64_t(blockIdx.x) >= cap || n >= end) return;
+    uint64_t* rec = buf + size_t(blockIdx.x) * kTraceSlots * 2;
     rec[2 * n] = t;
     rec[2 * n + 1] = (uint64_t(kind) << 56) | (uint64_t(a & 0xffffffu) << 32) | b;
     ++n;
@@ -244,13 +247,9 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
     *s_pf = 0;
     dev::mbar_init_fence();
   }
+  const uint64_t t_init = TraceLog::now();
   __syncthreads();
-  if (tid == 0) {
-    trace.init(0, kTraceProducerSlot0);
-    trace.entry(t_entry);
-  } else if (tid == T::kConsumers) {
-    trace.init(kTraceProducerSlot0, kTraceSlots);
-  }
+  const uint64_t t_sync = TraceLog::now();
 
   // A wait that failed: record it once, make every later wait of the CTA give
   // up at once, and carry on without waiting so that nothing hangs.
@@ -338,8 +337,19 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
   if (warp >= T::kConsumerWarps) {
     // ================================================ producer warpgroup
     if constexpr (T::kHandOver) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(T::kRegsProducer));
+    // (After the register hand-over: it would wait for the trace loads.)
+    if (tid == T::kConsumers) trace.init(kTraceProducerSlot0, kTraceSlots);
     const int pw = warp - T::kConsumerWarps;  // this warp owns A rows [32 pw, 32 pw + 32)
-    if (pw == 0 && lane == 0) trace.put(kTrProducerStart, 0, 0);
+    // Producer phase times, recorded when the producer is done (see TraceLog).
+    const uint64_t tp_start = TraceLog::now();
+    uint64_t tp_issued = 0, tp_first_a = 0;
+    auto put_producer_times = [&]() {
+      if (pw == 0 && lane == 0) {
+        trace.put_at(tp_start, kTrProducerStart, 0, 0);
+        if (tp_issued) trace.put_at(tp_issued, kTrProducerIssued, 0, 0);
+        if (tp_first_a) trace.put_at(tp_first_a, kTrFirstALanded, 0, 0);
+      }
+    };
     uint64_t* my_astage = astage + pw * T::S2;
     float* my_staging = sAst + pw * T::S2 * T::kAStagingFloats;
     if (lane == 0) {
@@ -369,6 +379,7 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
       if (*s_abort && pw == 0 && lane == 0)
         for (uint32_t k = (i > T::S ? i - T::S : 0); k < i; ++k)
           dev::mbar_wait(&full[k % T::S], (k / T::S) & 1u, limit);
+      put_producer_times();
       prefetch_partials();
       return;
     }
@@ -401,7 +412,7 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
       issue.advance(sc, ctas);
     }
     const uint32_t b_issued = issued;
-    if (pw == 0 && lane == 0) trace.put(kTrProducerIssued, 0, 0);
+    tp_issued = TraceLog::now();
     uint32_t i = 0;
     for (; proc.valid; ++i) {
       const uint32_t s = i % T::S, n = i / T::S;
@@ -412,7 +423,7 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
         if (pw == 0 && lane == 0 && !*s_abort) issue_b(proc, s);
       }
       if (!dev::mbar_wait_abortable(&my_astage[s2], n2 & 1u, limit, s_abort)) fail(kWaitTileStage);
-      if (i == 0 && pw == 0 && lane == 0) trace.put(kTrFirstALanded, 0, 0);
+      if (i == 0) tp_first_a = TraceLog::now();
       // Transpose this warp's 32 rows: staging [r][k] (64-byte swizzled rows:
       // 16-byte chunk q of row r sits at q ^ ((r >> 1) & 3)) -> ring [k][m].
       // Consecutive lanes write consecutive m: conflict-free 4-byte stores.
@@ -452,12 +463,14 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
         for (uint32_t k = (i > T::S ? i - T::S : 0); k < i; ++k)
           dev::mbar_wait(&full[k % T::S], (k / T::S) & 1u, limit);
     }
+    put_producer_times();
     prefetch_partials();
     return;
   }
 
   // ======================================================= consumer warps
   if constexpr (T::kHandOver) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(T::kRegsConsumer));
+  if (tid == 0) trace.init(0, kTraceProducerSlot0);
   const int tr = T::kPairedCols ? (lane & 3) : lane / T::kTC;
   const int tc = T::kPairedCols ? (((lane >> 3) << 1) | ((lane >> 2) & 1)) : lane % T::kTC;
   const int wm = warp % T::kWarpsM, wn = warp / T::kWarpsM;
@@ -734,7 +747,12 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
       }
     }
   }
-  if (tid == 0) trace.put(kTrExit, 0, 0);
+  if (tid == 0) {
+    trace.entry(t_entry);
+    trace.put_at(t_init, kTrBarriersReady, 0, 0);
+    trace.put_at(t_sync, kTrCtaSynced, 0, 0);
+    trace.put(kTrExit, 0, 0);
+  }
 }
 
 template <class T>

@@ -29,6 +29,8 @@ enum TraceKind : uint32_t {
                          //                                       2: partials prefetched
   kTrProducerStart = 10, // producer warpgroup running (registers handed over)
   kTrFirstALanded = 11,  // producer: its first A slice is in shared memory
+  kTrBarriersReady = 12, // thread 0 initialised the CTA's mbarriers
+  kTrCtaSynced = 13,     // thread 0 passed the CTA barrier after that
 };
 
 constexpr int kTraceSlots = 64;

@@ -30,7 +30,7 @@ import numpy as np
 
 # Record kinds (TraceKind in csrc/sgemm_trace.h).
 (ENTRY, FIRST_STAGE, KLOOP_END, STORE_END, PUBLISH_END, REDUCE_END, EXIT, PRODUCER_ISSUED,
- OWNER_WAIT, PRODUCER_START, FIRST_A_LANDED) = range(1, 12)
+ OWNER_WAIT, PRODUCER_START, FIRST_A_LANDED, BARRIERS_READY, CTA_SYNCED) = range(1, 14)
 SLOTS = 64            # records per CTA (kTraceSlots)
 PRODUCER_SLOT0 = 56   # producer records start here (kTraceProducerSlot0)
 FFMA_PER_CLK_PER_SM = 128
@@ -69,6 +69,8 @@ class CtaTrace:
     units: list[Unit] = field(default_factory=list)
     producer_start: int | None = None
     first_a_landed: int | None = None
+    barriers_ready: int | None = None
+    cta_synced: int | None = None
 
 
 def decode(words: np.ndarray, ctas: int) -> list[list[Event]]:
@@ -101,7 +103,9 @@ def per_cta(events: list[list[Event]]) -> list[CtaTrace]:
         prod = next((e.t for e in ev if e.kind == PRODUCER_ISSUED), None)
         ct = CtaTrace(c, entry.a, entry.t, first, None, prod,
                       producer_start=next((e.t for e in ev if e.kind == PRODUCER_START), None),
-                      first_a_landed=next((e.t for e in ev if e.kind == FIRST_A_LANDED), None))
+                      first_a_landed=next((e.t for e in ev if e.kind == FIRST_A_LANDED), None),
+                      barriers_ready=next((e.t for e in ev if e.kind == BARRIERS_READY), None),
+                      cta_synced=next((e.t for e in ev if e.kind == CTA_SYNCED), None))
         prev = first if first is not None else entry.t
         unit, mark = None, 0     # the unit in its epilogue, and the end of its last phase
         for e in ev:
@@ -163,6 +167,10 @@ def summarize(traces: list[CtaTrace], flops: float | None = None, mhz: float = 2
                                    if t.first_stage is not None),
         "producer_issue_us": _stats((t.producer_issued - t.entry) * us for t in traces
                                     if t.producer_issued is not None),
+        "barriers_ready_us": _stats((t.barriers_ready - t.entry) * us for t in traces
+                                    if t.barriers_ready is not None),
+        "cta_synced_us": _stats((t.cta_synced - t.entry) * us for t in traces
+                                if t.cta_synced is not None),
         "producer_start_us": _stats((t.producer_start - t.entry) * us for t in traces
                                     if t.producer_start is not None),
         "first_a_landed_us": _stats((t.first_a_landed - t.entry) * us for t in traces
@@ -226,7 +234,8 @@ def format_summary(s: dict) -> str:
     lines = [
         f"CTAs {s['ctas']}, first entry to last exit {s['span_us']:.2f} us, "
         f"entry skew {s['entry_skew_us']:.2f} us, exit skew {s['exit_skew_us']:.2f} us",
-        st("start_latency_us"), st("producer_start_us"), st("producer_issue_us"),
+        st("start_latency_us"), st("barriers_ready_us"), st("cta_synced_us"),
+        st("producer_start_us"), st("producer_issue_us"),
         st("first_a_landed_us"),
         f"{'ktile_us (weighted)':<22} {s['ktile_us']:.4f} us over {s['ktiles']} k-tiles",
         st("ktile_us_by_unit"), st("ktiles_per_cta", ""), st("units_per_cta", ""),

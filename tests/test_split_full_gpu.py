@@ -54,6 +54,12 @@ def _tile_of(variant, A, B, C):
     if variant == sg.AUTO:
         variant = sg.select_variant(A, B, C)
     if variant == sg.SPECIALIZED:
+        # The instance compiled for this shape: the tile whose plan it matches.
+        M, K = A.shape
+        N = B.shape[1]
+        for tile in TILE.values():
+            if tile and plan_util.plan(M, N, K, tile[0], tile[1], 16, _resident())["spec"] >= 0:
+                return tile
         return None
     return TILE[variant]
 
