@@ -647,15 +647,18 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
     }
     if (own_first && !last) {
       // The other sharers usually finish their parts at about the same time
-      // (a sharer whose whole share lies in this tile ends with it).  Waiting
-      // a little for their arrivals costs less than publishing this partial
-      // and reading it back, so poll the counter for up to kOwnerWaitNs; if
-      // they are not all in by then, publish as any sharer does.  The wait is
-      // bounded, so no CTA depends on another being resident.
+      // (a sharer whose whole share lies in this tile ends with it).  Where
+      // partials are prefetched, waiting a little for their arrivals costs
+      // less than publishing this partial and reading it back, so poll the
+      // counter for up to kOwnerWaitNs; if they are not all in by then,
+      // publish as any sharer does.  The wait is bounded, so no CTA depends on
+      // another being resident.  Without prefetching (128 x 256 tiles: no
+      // room for a 128 KB partial) the wait measured a loss: at 4096^3 a few
+      // owners waited it out behind a slower SM and then published anyway.
       if (tid == 0) {
         const int32_t* cnt = args.counters + u.t_sk;
         int seen = dev::ld_acquire_gpu(cnt);
-        if (seen != others) {
+        if (T::kPfSlots > 0 && seen != others) {
           const uint64_t t0 = dev::global_timer_ns();
           while (seen != others && dev::global_timer_ns() - t0 < kOwnerWaitNs) {
             __nanosleep(64);
