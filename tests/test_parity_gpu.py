@@ -412,3 +412,30 @@ def test_timeout_on_one_stream_leaves_other_streams_running():
     ref, E = oracle.sgemm_f64(A_h, B_h)
     check_within_bound(first.cpu().numpy(), ref, E, w.K, "stream-K beside an expiring wait")
     assert sg.query_device_status() == (0, 0)
+
+
+def test_split_tile_handoffs_under_concurrent_kernels():
+    """Stream-K calls on four streams at once compete for SMs, so some CTAs of a launch start
+    late: owners then give up waiting for their sharers, the partial prefetch gives up, and
+    other CTAs finish the split tiles.  Whoever finishes, the sums are added in the same
+    order, so every result must equal the sequential one bit for bit."""
+    w = workloads.SQUARE_1024
+    A_h, B_h = workloads.operands(w)
+    A, B = A_h.cuda(), B_h.cuda()
+    ref = {v: sg.sgemm(A, B, variant=v) for v in (sg.STREAMK_SMALL, sg.SPECIALIZED, sg.STREAMK)}
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    outs = []
+    for rep in range(6):
+        for i, s in enumerate(streams):
+            v = (sg.STREAMK_SMALL, sg.SPECIALIZED, sg.STREAMK)[(rep + i) % 3]
+            with torch.cuda.stream(s):
+                C = torch.full((w.M, w.N), float("nan"), device="cuda")
+                sg.sgemm(A, B, out=C, variant=v)
+            outs.append((v, C))
+    torch.cuda.synchronize()
+    assert sg.query_device_status() == (0, 0)
+    for k, (v, C) in enumerate(outs):
+        assert torch.equal(C, ref[v]), f"call {k} (variant {v}) differs from the sequential result"
+    E_ref, E = oracle.sgemm_f64(A_h, B_h)
+    check_within_bound(ref[sg.STREAMK_SMALL].cpu().numpy(), E_ref, E, w.K, "concurrent hand-offs")
