@@ -437,5 +437,5 @@ def test_split_tile_handoffs_under_concurrent_kernels():
     assert sg.query_device_status() == (0, 0)
     for k, (v, C) in enumerate(outs):
         assert torch.equal(C, ref[v]), f"call {k} (variant {v}) differs from the sequential result"
-    E_ref, E = oracle.sgemm_f64(A_h, B_h)
-    check_within_bound(ref[sg.STREAMK_SMALL].cpu().numpy(), E_ref, E, w.K, "concurrent hand-offs")
+    C_ref, E = oracle.sgemm_f64(A_h, B_h)
+    check_within_bound(ref[sg.STREAMK_SMALL].cpu().numpy(), C_ref, E, w.K, "concurrent hand-offs")
