@@ -535,13 +535,17 @@ def run_ours(args):
 
     if args.sweep:
         for w in sweep_plan(workloads.ALL, args.out):
-            A_h, B_h, _, _, C, times, chosen = bench_workload(w, args, sg, device, flush, variant)
+            with ClockSampler(local) as clocks:
+                A_h, B_h, _, _, C, times, chosen = bench_workload(w, args, sg, device, flush, variant)
+            clock = clocks.summary()
             ms = statistics.median(times)
             line = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
                     "variant": sg.variant_name(chosen), "us_median": ms * 1e3,
                     "us_p10": sorted(times)[len(times) // 10] * 1e3,
                     "us_p90": sorted(times)[(9 * len(times)) // 10] * 1e3,
-                    "tflops": w.flops / (ms * 1e-3) / 1e12}
+                    "tflops": w.flops / (ms * 1e-3) / 1e12,
+                    "clocks": {"sm_mhz": clock["sm_mhz"], "sm_max_mhz": clock["sm_max_mhz"],
+                               "reasons": clock["reasons"], "samples": clock["samples"]}}
             if args.sweep_cpu_seconds > 0 and rank == 0:
                 # The oracle on the host cores, a reported baseline only: all cores for
                 # every workload, one core as well up to 1024^3.
