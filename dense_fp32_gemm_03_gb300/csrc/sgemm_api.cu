@@ -382,9 +382,13 @@ enum OpMode {
   kTranspose,  // copied into the workspace transposed (transpose kernel)
 };
 
+// The pipelined variants read a transposed A in place when their tile
+// configuration has the M-major instance (the default ones do).
 bool reads_a_mn(int v) {
-  return v == SGEMM_VARIANT_TILED || v == SGEMM_VARIANT_STREAMK || v == SGEMM_VARIANT_TILED_SMALL ||
-         v == SGEMM_VARIANT_STREAMK_SMALL;
+  if (v == SGEMM_VARIANT_TILED || v == SGEMM_VARIANT_STREAMK) return gb300::tile_shape(g_cfg_large).a_mn;
+  if (v == SGEMM_VARIANT_TILED_SMALL || v == SGEMM_VARIANT_STREAMK_SMALL)
+    return gb300::tile_shape(g_cfg_small).a_mn;
+  return false;
 }
 
 OpMode a_mode(int v, bool trans_a, bool aligned) {

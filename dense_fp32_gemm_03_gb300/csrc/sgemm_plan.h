@@ -133,6 +133,7 @@ struct TileShape {
   int a_box_rows;  // rows of A per TMA copy (one producer warp's slice)
   int patch_n;     // outputs per thread along N (16 or 8)
   int ctas_per_sm; // CTAs the configuration is built to co-reside per SM
+  bool a_mn;       // has an instance that reads A M-major (GemmArgs::a_mn)
 };
 
 TileShape tile_shape(TileConfig cfg);

@@ -41,6 +41,7 @@
 #include <cuda_runtime.h>
 
 #include <tuple>
+#include <type_traits>
 #include <utility>
 
 #include "sgemm_device.cuh"
@@ -181,6 +182,11 @@ using Cfg2 = TileCfg<4, 2, 16, 6, 4, true, 1, 56, true>;    // Cfg1 with fragmen
 using Cfg3 = TileCfg<4, 2, 8, 4, 4, true, 1, 56, false, 1>; // 128 x 128 tile, 8 + 4 warps, 8x8 patch
 using Cfg4 = TileCfg<4, 2, 8, 4, 4, true, 1, 56, true>;     // Cfg3, paired-column lane layout
 using Cfg5 = TileCfg<4, 2, 8, 4, 4, false, 1, 56, true>;    // Cfg4 without double buffering
+
+// Only the configurations the selector uses by default (0 and 3) carry
+// instances that read A M-major; the others exist for tuning runs.
+template <class T>
+constexpr bool kHasAmn = std::is_same<T, Cfg0>::value || std::is_same<T, Cfg3>::value;
 
 template <class F>
 auto with_cfg(int id, F&& f) {
@@ -763,12 +769,15 @@ int prepare() {
   if (cudaFuncSetAttribute(tile_kernel<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(T::kSmem)) != cudaSuccess ||
       cudaFuncSetAttribute(tile_kernel<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           int(T::kSmem)) != cudaSuccess ||
-      cudaFuncSetAttribute(tile_kernel<T, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           int(T::kSmem)) != cudaSuccess ||
-      cudaFuncSetAttribute(tile_kernel<T, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(T::kSmem)) != cudaSuccess)
     return -1;
+  if constexpr (kHasAmn<T>) {
+    if (cudaFuncSetAttribute(tile_kernel<T, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(T::kSmem)) != cudaSuccess ||
+        cudaFuncSetAttribute(tile_kernel<T, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(T::kSmem)) != cudaSuccess)
+      return -1;
+  }
   int blocks = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, tile_kernel<T, false>, T::NT,
                                                     T::kSmem) != cudaSuccess)
@@ -851,7 +860,7 @@ bool spec_launch_at(int i, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
 template <class T>
 TileShape shape_of() {
   return TileShape{T::BM, T::BN, T::BK, T::NT, T::S, T::kSmem, T::kRowsPerProducer, T::kTN,
-                   T::kCtasPerSm};
+                   T::kCtasPerSm, kHasAmn<T>};
 }
 
 }  // namespace
@@ -886,10 +895,14 @@ cudaError_t launch_tile_kernel(TileConfig cfg, const CUtensorMap& tmap_a, const 
     using T = decltype(c);
     const bool scaled = args.scaled || args.c_scalar;
     if (args.a_mn) {
-      if (scaled)
-        tile_kernel<T, true, true><<<grid, T::NT, T::kSmem, stream>>>(tmap_a, tmap_b, args, sched);
-      else
-        tile_kernel<T, false, true><<<grid, T::NT, T::kSmem, stream>>>(tmap_a, tmap_b, args, sched);
+      if constexpr (kHasAmn<T>) {
+        if (scaled)
+          tile_kernel<T, true, true><<<grid, T::NT, T::kSmem, stream>>>(tmap_a, tmap_b, args, sched);
+        else
+          tile_kernel<T, false, true><<<grid, T::NT, T::kSmem, stream>>>(tmap_a, tmap_b, args, sched);
+      } else {
+        return cudaErrorInvalidValue;  // the host reads tile_shape().a_mn first
+      }
     } else if (scaled) {
       tile_kernel<T, true><<<grid, T::NT, T::kSmem, stream>>>(tmap_a, tmap_b, args, sched);
     } else {
