@@ -143,8 +143,10 @@ def _check_op(got, opA, opB, A_st, B_st, ta, tb, alpha, beta, C0, what, col_majo
 # 1024^3 size (size-specialized instance when nothing is copied), the
 # small-product kernel, ragged sizes whose transposed storage has row strides
 # that are not multiples of 4 (copied, or the guarded kernel), and a thin one.
+# 1023 x 1025 x 515: every stored matrix has an odd row stride, so the staged
+# variant copies the operands: transposed copies and aligned copies together.
 OP_SHAPES = [(1536, 1536, 512), (1024, 1024, 1024), (256, 512, 64), (300, 520, 200),
-             (129, 77, 33), (1000, 1000, 100), (64, 4096, 256)]
+             (129, 77, 33), (1000, 1000, 100), (64, 4096, 256), (1023, 1025, 515)]
 
 
 @pytest.mark.parametrize("shape", OP_SHAPES, ids=lambda s: "x".join(map(str, s)))
