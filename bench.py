@@ -8,7 +8,7 @@ before every timed step by writing a buffer twice the L2 size, and every step
 is timed with CUDA events on the launching stream (the flush is outside the
 events), as in "Beyond Kernel 7", section "The confirmed result".
 Throughput counts 2*M*N*K operations per call (an FFMA counts as two).
-At 1024^3 and 4096^3 (and the sweep's 768^3, 1536^3 and 2048^3) the selector
+At 1024^3 and 4096^3 (and the sweep's 768^3) the selector
 takes a size-specialized kernel instance (shape and schedule compiled in); the
 best generic variant is timed on the same protocol and reported beside it
 under ``generic``.

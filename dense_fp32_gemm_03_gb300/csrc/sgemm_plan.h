@@ -159,10 +159,9 @@ struct SpecShape {
 };
 // The compiled instances, by index (the kernel translation unit checks that
 // its instance list matches this table).  768^3 and 1024^3 run 128 x 128
-// tiles (configuration 3), the larger sizes 128 x 256 (configuration 0).
+// tiles (configuration 3), 4096^3 128 x 256 (configuration 0).
 constexpr SpecShape kSpecShapes[] = {{0, 4096, 4096, 4096}, {3, 1024, 1024, 1024},
-                                     {3, 768, 768, 768},    {0, 1536, 1536, 1536},
-                                     {0, 2048, 2048, 2048}};
+                                     {3, 768, 768, 768}};
 constexpr int kSpecShapeCount = int(sizeof(kSpecShapes) / sizeof(kSpecShapes[0]));
 
 // The instance compiled for exactly this launch -- configuration `cfg` with

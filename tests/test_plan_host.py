@@ -129,8 +129,7 @@ def test_split_tiles_have_distinct_slots(probe):
 
 # The size-specialized instances (kSpecShapes in sgemm_plan.h): shape and tile.
 SPECIALIZED = [((4096, 4096, 4096), (128, 256)), ((1024, 1024, 1024), (128, 128)),
-               ((768, 768, 768), (128, 128)), ((1536, 1536, 1536), (128, 256)),
-               ((2048, 2048, 2048), (128, 256))]
+               ((768, 768, 768), (128, 128))]
 
 
 def test_specialized_instance_needs_the_compiled_sm_count(probe):
@@ -147,6 +146,7 @@ def test_specialized_instance_needs_the_compiled_sm_count(probe):
 def test_specialized_instance_only_for_its_shape_and_tile(probe):
     cs = [(4096, 4096, 4092, 128, 256, 16, 152, True), (1024, 1024, 2048, 128, 128, 16, 152, True),
           (1024, 1024, 1024, 128, 256, 16, 152, True), (4096, 4096, 4096, 128, 128, 16, 152, True),
-          (2048, 2048, 2048, 128, 256, 16, 152, False), (1023, 1024, 1024, 128, 128, 16, 152, True)]
+          (2048, 2048, 2048, 128, 256, 16, 152, False), (1023, 1024, 1024, 128, 128, 16, 152, True),
+          (2048, 2048, 2048, 128, 256, 16, 152, True), (1536, 1536, 1536, 128, 256, 16, 152, True)]
     for case, p in zip(cs, probe(cs)):
         assert p["spec"] == -1, case

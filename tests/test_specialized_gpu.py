@@ -1,4 +1,4 @@
-"""GPU parity of the size-specialized instances (M = N = K = 768, 1024, 1536, 2048, 4096).
+"""GPU parity of the size-specialized instances (M = N = K = 768, 1024, 4096).
 
 The specialized instance runs the same Stream-K schedule as the generic
 kernel with the shape compiled in, so its output must equal the generic
@@ -36,10 +36,8 @@ def _sweep(n):
 
 @pytest.mark.parametrize("w,generic", [(_sweep(768), sg.STREAMK_SMALL),
                                        (workloads.SQUARE_1024, sg.STREAMK_SMALL),
-                                       (_sweep(1536), sg.STREAMK),
-                                       (_sweep(2048), sg.STREAMK),
                                        (workloads.SQUARE_4096, sg.STREAMK)],
-                         ids=["768", "1024", "1536", "2048", "4096"])
+                         ids=["768", "1024", "4096"])
 def test_selected_and_bit_identical_to_generic(w, generic):
     A, B = (x.cuda() for x in workloads.operands(w))
     C_spec = torch.full((w.M, w.N), float("nan"), device="cuda")
@@ -70,19 +68,6 @@ def test_768_full_compare():
     check_within_bound(C.cpu().numpy(), ref, E, w.K, "768^3 specialized")
 
 
-@pytest.mark.parametrize("n", [1536, 2048])
-def test_sweep_sizes_sampled_and_last_tile_row(n):
-    w = _sweep(n)
-    A, B = workloads.operands(w)
-    C = sg.sgemm(A.cuda(), B.cuda(), variant=sg.SPECIALIZED).cpu().numpy()
-    r, c = workloads.sample_indices(w.M, w.N, 4096, w.seed)
-    ref, E = oracle.sgemm_entries_f64(A, B, r.numpy(), c.numpy())
-    check_within_bound(C[r.numpy(), c.numpy()], ref, E, w.K, f"{n}^3 specialized (sampled)")
-    rows = slice(n - 128, n)
-    ref, E = oracle.sgemm_f64(A[rows], B)
-    check_within_bound(C[rows], ref, E, w.K, f"{n}^3 specialized, last tile row")
-
-
 def test_4096_sampled_and_row_block():
     w = workloads.SQUARE_4096
     A, B = workloads.operands(w)
@@ -106,7 +91,8 @@ def test_integer_inputs_exact_at_1024():
 
 
 @pytest.mark.parametrize("shape", [(512, 512, 512), (1024, 1024, 1020), (4096, 4096, 4092),
-                                   (1024, 1024, 2048)], ids=lambda s: "x".join(map(str, s)))
+                                   (1024, 1024, 2048), (1536, 1536, 1536), (2048, 2048, 2048)],
+                         ids=lambda s: "x".join(map(str, s)))
 def test_other_shapes_unsupported(shape):
     M, N, K = shape
     A = torch.zeros(M, K, device="cuda")

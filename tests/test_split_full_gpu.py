@@ -6,7 +6,8 @@ compared element by element at the configurations' full sizes:
 * 1024 x 1024 x 16384 (long K): every tile is split, so the whole product is
   compared, through the selector, Stream-K on 128 x 256 tiles and Stream-K on
   128 x 128 tiles;
-* 16384 x 1024 x 4096 (tall), 8192^3 and 4096^3: whole tile-row blocks that hold
+* 16384 x 1024 x 4096 (tall), 8192^3, 4096^3 and the sweep's 1536^3 and 2048^3
+  (every tile split): whole tile-row blocks that hold
   split tiles.  The blocks are chosen from the schedule itself (plan_launch,
   read through tests/plan_probe.cpp): the test asserts that each block
   contains split tiles of the variant it runs.
@@ -81,8 +82,11 @@ def test_long_k_every_tile_split_full_compare():
         check_within_bound(C.cpu().numpy(), ref, E, w.K, f"{w.name} variant {v} (full)")
 
 
-@pytest.mark.parametrize("w", [workloads.TALL, workloads.SQUARE_8192, workloads.SQUARE_4096],
-                         ids=lambda w: w.name)
+SWEEP_LARGE = [s for s in workloads.SWEEP if s.M in (1536, 2048)]
+
+
+@pytest.mark.parametrize("w", [workloads.TALL, workloads.SQUARE_8192, workloads.SQUARE_4096,
+                               *SWEEP_LARGE], ids=lambda w: w.name)
 @pytest.mark.parametrize("variant", [sg.AUTO, sg.STREAMK], ids=["auto", "streamk"])
 def test_row_blocks_with_split_tiles(w, variant):
     A_h, B_h = workloads.operands(w)
