@@ -24,7 +24,8 @@ VARIANTS = {"guarded": GUARDED, "tiled": TILED, "streamk": STREAMK,
 # Every entry point include/sgemm.h declares.
 EXPORTS = ("sgemm", "sgemm_variant", "sgemm_select_variant", "sgemm_workspace_size",
            "sgemm_query_device_status", "sgemm_release_workspaces", "sgemm_status_string",
-           "sgemm_variant_name", "sgemm_debug_expire_wait", "sgemm_streamk_static",
+           "sgemm_variant_name", "sgemm_debug_expire_wait", "sgemm_debug_owner_publishes",
+           "sgemm_streamk_static",
            "sgemm_tf32", "sgemm_ex", "sgemm_ex2")
 
 
@@ -75,6 +76,8 @@ def load(path: str | None = None):
         lib.sgemm_variant_name.restype = ctypes.c_char_p
         lib.sgemm_debug_expire_wait.argtypes = [ctypes.c_uint64, vp]
         lib.sgemm_debug_expire_wait.restype = st
+        lib.sgemm_debug_owner_publishes.argtypes = [ctypes.c_int]
+        lib.sgemm_debug_owner_publishes.restype = None
         lib.sgemm_streamk_static.argtypes = gemm_args
         lib.sgemm_streamk_static.restype = st
         lib.sgemm_tf32.argtypes = gemm_args
@@ -271,6 +274,11 @@ def debug_expire_wait(limit_ns: int, stream=None) -> int:
     import torch
     return load().sgemm_debug_expire_wait(int(limit_ns),
                                           _stream_handle(torch.cuda.current_device(), stream))
+
+
+def debug_owner_publishes(on: bool) -> None:
+    """Test switch: split tiles are always summed from the workspace (see include/sgemm.h)."""
+    load().sgemm_debug_owner_publishes(1 if on else 0)
 
 
 def sgemm_streamk_static_raw(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:

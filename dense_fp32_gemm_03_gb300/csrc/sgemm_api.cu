@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -26,6 +27,9 @@ using gb300::TileShape;
 // [0] = first sgemm_status_t recorded by a kernel since the last query, [1] = wait site;
 // [2..3] = the snapshot a query takes of [0..1] (status_take_kernel).
 __device__ uint32_t g_status_word[4];
+
+// sgemm_debug_owner_publishes(): copied into every pipelined launch's arguments.
+std::atomic<int> g_owner_publishes{0};
 
 constexpr int64_t kInt32Max = 0x7fffffffLL;
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
@@ -674,6 +678,7 @@ sgemm_status_t run(int variant, int64_t M, int64_t N, int64_t K, float alpha, co
   args.beta = beta;
   args.c_scalar = c_ok ? 0 : 1;
   args.a_mn = a_mn ? 1 : 0;
+  args.owner_publishes = g_owner_publishes.load(std::memory_order_relaxed);
   const cudaError_t e =
       spec >= 0 ? gb300::launch_specialized(spec, tmap_a, tmap_b, args, p.sc, p.grid, stream)
                 : gb300::launch_tile_kernel(p.cfg, tmap_a, tmap_b, args, p.sc, p.grid, stream);
@@ -949,6 +954,10 @@ const char* sgemm_variant_name(int v) {
   return "unknown";
 }
 
+void sgemm_debug_owner_publishes(int on) {
+  g_owner_publishes.store(on ? 1 : 0, std::memory_order_relaxed);
+}
+
 sgemm_status_t sgemm_debug_expire_wait(uint64_t limit_ns, cudaStream_t stream) {
   DeviceState* ds = nullptr;
   sgemm_status_t st = device_state(&ds, nullptr);
@@ -1041,6 +1050,7 @@ extern "C" sgemm_status_t sgemm_streamk_static(int64_t M, int64_t N, int64_t K, 
   args.partials = reinterpret_cast<float*>(static_cast<char*>(scratch) + kCounterBytes);
   args.status = ds->status;
   args.wait_limit_ns = kDefaultWaitLimitNs;
+  args.owner_publishes = g_owner_publishes.load(std::memory_order_relaxed);
   return gb300::launch_tile_kernel(p.cfg, tmap_a, tmap_b, args, p.sc, p.grid, stream) == cudaSuccess
              ? SGEMM_OK
              : SGEMM_ERR_LAUNCH;

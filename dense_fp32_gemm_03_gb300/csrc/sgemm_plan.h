@@ -121,6 +121,11 @@ struct GemmArgs {
   // fastest): tmap_a then has box {BM, BK} and its copies land in the A ring
   // as the compute warps read it, with no staging and no transposition.
   int32_t a_mn;
+  // Test switch: nonzero makes the CTA that owns a split tile's first
+  // k-tiles publish its partial like every other sharer, so the last to arrive
+  // always sums all partials from the workspace (the same additions, in CTA
+  // order, as the owner's sum from its registers).
+  int32_t owner_publishes;
 };
 
 // Tile configurations of the pipelined kernel (compiled instances, by id).

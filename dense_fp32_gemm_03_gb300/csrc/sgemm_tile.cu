@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
       int c_first, c_last;
       sharers(lu.t_sk, c_first, c_last);
       const int others = c_last - c_first;
-      if (c_first != cta || others == 0) return;
+      if (c_first != cta || others == 0 || args.owner_publishes) return;
       int npf = 0;
       if (!*s_abort) {
         const int32_t* cnt = args.counters + lu.t_sk;
@@ -635,7 +635,7 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
     sharers(u.t_sk, c_first, c_last);
     const int others = c_last - c_first;
     const int64_t tile_floats = int64_t(T::BM) * T::BN;
-    const bool own_first = cta == c_first;
+    const bool own_first = cta == c_first && !args.owner_publishes;
     bool last = false;
     int npf = 0;  // other sharers' partials already in shared memory
     if constexpr (T::kPfSlots > 0) {
@@ -699,21 +699,11 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
       const float4* base = reinterpret_cast<const float4*>(args.partials) + tid;
       const int64_t slot_vec = tile_floats / 4;
       if (own_first) {
-        // acc += partial, CTA after CTA, with a slot's loads in flight at once.
-#pragma unroll 1
-        for (int cc = c_first + 1; cc <= c_last; ++cc) {
-          float4 v[T::kOutVec];
-          if (cc - c_first - 1 < npf) {
-            const float4* src = reinterpret_cast<const float4*>(
-                                    smem + T::kPfOff + size_t(cc - c_first - 1) * T::kSlotBytes) +
-                                tid;
-#pragma unroll
-            for (int j = 0; j < T::kOutVec; ++j) v[j] = src[j * T::kConsumers];
-          } else {
-            const float4* src = base + (u.t_sk + cc) * slot_vec;
-#pragma unroll
-            for (int j = 0; j < T::kOutVec; ++j) v[j] = __ldcg(src + j * T::kConsumers);
-          }
+        // acc += partial, CTA after CTA.  Partials in shared memory first (the
+        // prefetched ones lead in CTA order), then the rest from L2 with a
+        // slot's loads in flight at once -- two slots' where the registers
+        // allow (the additions keep CTA order either way).
+        auto add_partial = [&](const float4 (&v)[T::kOutVec]) {
 #pragma unroll
           for (int j = 0; j < T::kOutVec; ++j) {
             const int r = j / Q, h = j % Q;
@@ -722,23 +712,47 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
             acc[r][2 * h + 1].x += v[j].z;
             acc[r][2 * h + 1].y += v[j].w;
           }
+        };
+        int cc = c_first + 1;
+#pragma unroll 1
+        for (; cc <= c_last && cc - c_first - 1 < npf; ++cc) {
+          float4 v[T::kOutVec];
+          const float4* src = reinterpret_cast<const float4*>(
+                                  smem + T::kPfOff + size_t(cc - c_first - 1) * T::kSlotBytes) +
+                              tid;
+#pragma unroll
+          for (int j = 0; j < T::kOutVec; ++j) v[j] = src[j * T::kConsumers];
+          add_partial(v);
+        }
+        if constexpr (T::kOutVec <= 16) {
+#pragma unroll 1
+          for (; cc + 1 <= c_last; cc += 2) {
+            float4 v0[T::kOutVec], v1[T::kOutVec];
+            const float4* src0 = base + (u.t_sk + cc) * slot_vec;
+            const float4* src1 = src0 + slot_vec;
+#pragma unroll
+            for (int j = 0; j < T::kOutVec; ++j) v0[j] = __ldcg(src0 + j * T::kConsumers);
+#pragma unroll
+            for (int j = 0; j < T::kOutVec; ++j) v1[j] = __ldcg(src1 + j * T::kConsumers);
+            add_partial(v0);
+            add_partial(v1);
+          }
+        }
+#pragma unroll 1
+        for (; cc <= c_last; ++cc) {
+          float4 v[T::kOutVec];
+          const float4* src = base + (u.t_sk + cc) * slot_vec;
+#pragma unroll
+          for (int j = 0; j < T::kOutVec; ++j) v[j] = __ldcg(src + j * T::kConsumers);
+          add_partial(v);
         }
 #pragma unroll
         for (int j = 0; j < T::kOutVec; ++j) store_c(j, value(j));
       } else {
-        // Sum every partial, this CTA's included, in CTA order.
+        // Sum every partial, this CTA's included, in CTA order (two slots'
+        // loads in flight at once where the registers allow).
         float4 sum[T::kOutVec];
-        {
-          const float4* src = base + (u.t_sk + c_first) * slot_vec;
-#pragma unroll
-          for (int j = 0; j < T::kOutVec; ++j) sum[j] = __ldcg(src + j * T::kConsumers);
-        }
-#pragma unroll 1
-        for (int cc = c_first + 1; cc <= c_last; ++cc) {
-          const float4* src = base + (u.t_sk + cc) * slot_vec;
-          float4 v[T::kOutVec];
-#pragma unroll
-          for (int j = 0; j < T::kOutVec; ++j) v[j] = __ldcg(src + j * T::kConsumers);
+        auto add_partial = [&](const float4 (&v)[T::kOutVec]) {
 #pragma unroll
           for (int j = 0; j < T::kOutVec; ++j) {
             sum[j].x += v[j].x;
@@ -746,6 +760,34 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
             sum[j].z += v[j].z;
             sum[j].w += v[j].w;
           }
+        };
+        {
+          const float4* src = base + (u.t_sk + c_first) * slot_vec;
+#pragma unroll
+          for (int j = 0; j < T::kOutVec; ++j) sum[j] = __ldcg(src + j * T::kConsumers);
+        }
+        int cc = c_first + 1;
+        if constexpr (T::kOutVec <= 16) {
+#pragma unroll 1
+          for (; cc + 1 <= c_last; cc += 2) {
+            float4 v0[T::kOutVec], v1[T::kOutVec];
+            const float4* src0 = base + (u.t_sk + cc) * slot_vec;
+            const float4* src1 = src0 + slot_vec;
+#pragma unroll
+            for (int j = 0; j < T::kOutVec; ++j) v0[j] = __ldcg(src0 + j * T::kConsumers);
+#pragma unroll
+            for (int j = 0; j < T::kOutVec; ++j) v1[j] = __ldcg(src1 + j * T::kConsumers);
+            add_partial(v0);
+            add_partial(v1);
+          }
+        }
+#pragma unroll 1
+        for (; cc <= c_last; ++cc) {
+          const float4* src = base + (u.t_sk + cc) * slot_vec;
+          float4 v[T::kOutVec];
+#pragma unroll
+          for (int j = 0; j < T::kOutVec; ++j) v[j] = __ldcg(src + j * T::kConsumers);
+          add_partial(v);
         }
 #pragma unroll
         for (int j = 0; j < T::kOutVec; ++j) store_c(j, sum[j]);

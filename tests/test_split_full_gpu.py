@@ -112,3 +112,76 @@ def test_row_blocks_with_split_tiles(w, variant):
         ref, E = oracle.sgemm_f64(A_h[rows], B_h)
         check_within_bound(got[rows], ref, E, w.K,
                            f"{w.name} variant {variant} tile row {tm} ({len(in_block)} split tiles)")
+
+
+# The owner of a split tile normally keeps its partial in registers and adds
+# the other sharers' partials to it; with the test switch every sharer
+# publishes and the last to arrive sums all partials from the workspace.  Both
+# paths add the same partials in CTA order, so the results must be equal bit
+# for bit.  The shapes cover both tile configurations, the size-specialized
+# instances, ragged edges, up to five sharers of a tile (768^3) and the scaled
+# epilogue.
+SUM_PATHS = [((1024, 1024, 1024), sg.AUTO), ((1024, 1024, 1024), sg.STREAMK_SMALL),
+             ((1024, 1024, 1024), sg.STREAMK), ((768, 768, 768), sg.AUTO),
+             ((768, 768, 768), sg.STREAMK_SMALL), ((1000, 1100, 900), sg.STREAMK_SMALL),
+             ((1000, 1100, 900), sg.STREAMK), ((1024, 1024, 16384), sg.STREAMK),
+             ((4096, 4096, 4096), sg.AUTO)]
+
+
+def _with_owner_publishing(fn):
+    sg.debug_owner_publishes(True)
+    try:
+        return fn()
+    finally:
+        sg.debug_owner_publishes(False)
+
+
+@pytest.mark.parametrize("shape,variant", SUM_PATHS,
+                         ids=[f"{'x'.join(map(str, s))}-{sg.variant_name(v) if v >= 0 else 'auto'}"
+                              for s, v in SUM_PATHS])
+def test_split_tiles_summed_from_the_workspace_match_bit_for_bit(shape, variant):
+    M, N, K = shape
+    w = workloads.Workload(f"sumpath_{M}x{N}x{K}", M, N, K, "uniform", 2300 + M + K)
+    A_h, B_h = workloads.operands(w)
+    A, B = A_h.cuda(), B_h.cuda()
+    C = torch.empty(M, N, device="cuda")
+    tile = _tile_of(variant, A, B, C)
+    assert tile is not None
+    assert list(plan_util.split_tiles(plan_util.plan(M, N, K, tile[0], tile[1], 16, _resident()))), \
+        "the schedule splits no tile"
+    default = sg.sgemm(A, B, variant=variant)
+    published = _with_owner_publishing(lambda: sg.sgemm(A, B, variant=variant))
+    torch.cuda.synchronize()
+    assert torch.equal(default, published)
+    r, c = workloads.sample_indices(M, N, 2048, w.seed)
+    ref, E = oracle.sgemm_entries_f64(A_h, B_h, r.numpy(), c.numpy())
+    check_within_bound(published[r.cuda(), c.cuda()].cpu().numpy(), ref, E, K,
+                       f"{w.name} variant {variant}, every partial from the workspace")
+
+
+def test_split_tiles_summed_from_the_workspace_scaled_and_static():
+    """The same equality through the scaled epilogue and the allocation-free entry point."""
+    M = N = K = 1024
+    w = workloads.Workload("sumpath_scaled_1024", M, N, K, "uniform", 2399)
+    A_h, B_h = workloads.operands(w)
+    A, B = A_h.cuda(), B_h.cuda()
+    C0 = torch.randn(M, N, device="cuda")
+
+    def scaled():
+        C = C0.clone()
+        sg.sgemm_ex(A, B, C, alpha=0.75, beta=-1.5)
+        return C
+
+    def static():
+        C = torch.empty(M, N, device="cuda")
+        st = sg.binding.sgemm_streamk_static_raw(M, N, K, A.data_ptr(), K, B.data_ptr(), N,
+                                                 C.data_ptr(), N,
+                                                 torch.cuda.current_stream().cuda_stream)
+        assert st == 0, st
+        return C
+
+    for fn in (scaled, static):
+        default = fn()
+        published = _with_owner_publishing(fn)
+        torch.cuda.synchronize()
+        assert torch.equal(default, published), fn.__name__
