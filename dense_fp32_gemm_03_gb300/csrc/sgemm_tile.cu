@@ -237,6 +237,7 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
 
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
+  constexpr bool kEarlyFirstCopy = !AMN && FM > 0;
   const int cta = blockIdx.x, ctas = gridDim.x;
   const uint64_t limit = args.wait_limit_ns;
   TraceLog trace;
@@ -252,6 +253,25 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
     *s_epi = 0;
     *s_pf = 0;
     dev::mbar_init_fence();
+    // Size-specialized instances: the first k-tile's copies leave now, before
+    // the CTA-wide barrier and the producers' register hand-over (right after
+    // a cache flush they wait on DRAM, and that wait starts the pipeline); the
+    // producers issue the rest.  The generic kernel would first wait here for
+    // its schedule in the constant bank, which measured slower.
+    if constexpr (kEarlyFirstCopy) {
+      KCursor c0;
+      c0.init(sc, cta, ctas);
+      if (c0.valid) {
+        const int k0 = c0.u.kb * T::BK;
+        for (int pw = 0; pw < T::kProducerWarps; ++pw) {
+          dev::mbar_arrive_expect_tx(&astage[pw * T::S2], T::kAStagingBytes);
+          dev::tma_load_2d(sAst + pw * T::S2 * T::kAStagingFloats, &tmap_a, k0,
+                           c0.tm * T::BM + pw * T::kRowsPerProducer, &astage[pw * T::S2]);
+        }
+        dev::mbar_expect_tx(&full[0], T::kBStageBytes);
+        dev::tma_load_2d(sB, &tmap_b, c0.tn * T::BN, k0, &full[0]);
+      }
+    }
   }
   const uint64_t t_init = TraceLog::now();
   __syncthreads();
@@ -407,10 +427,11 @@ __global__ void __launch_bounds__(T::NT, T::kCtasPerSm)
     // Prologue: this warp's first S2 A slices into its staging ring and, from
     // warp 0, the B tiles of the same k-tiles (their ring stages start empty),
     // each right behind its A slice so that the first stage fills as early
-    // as the copies allow.
+    // as the copies allow.  (With kEarlyFirstCopy the first k-tile's copies
+    // were issued at set-up.)
     uint32_t issued = 0;
     for (int s = 0; s < T::S2 && issue.valid; ++s) {
-      if (lane == 0) {
+      if (lane == 0 && (s > 0 || !kEarlyFirstCopy)) {
         issue_a(s);
         if (pw == 0) issue_b(issue, s);
       }
