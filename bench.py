@@ -13,9 +13,10 @@ takes a size-specialized kernel instance (shape and schedule compiled in); the
 best generic variant is timed on the same protocol and reported beside it
 under ``generic``.
 
-Also reported: the same metric end to end through the C ABI with pinned host
-buffers (host-to-device copies of A and B and the device-to-host copy of C
-inside each timed step), the 1024^3 problem as a secondary figure, the
+Also reported: the same metric end to end through the C-ABI call with host
+buffers, ``sgemm_host`` (pinned A, B and C; the host-to-device copies of A and
+B and the device-to-host copy of C happen inside each timed call, overlapped
+with the multiply in row panels), the 1024^3 problem as a secondary figure, the
 roofline position of the tile kernel against the FP32 FFMA peak
 (SMs x 128 FFMA/clk x 2 FLOP x clock), and the CPU oracle timed on a bounded
 row sample of the same problem on the host cores.
@@ -376,74 +377,54 @@ def generic_figure(w, args, sg, device, flush, chosen):
             "unit": UNIT, "us_median": best[1], "steps": sub.steps}
 
 
-def e2e_pipelined(w, sg, device, variant, A_h, B_h, steps, warmup):
-    """Seconds for ``steps`` end-to-end steps: H2D of A and B from pinned host memory, the
-    C-ABI multiply, D2H of C; copies and compute on separate streams, two buffer sets."""
+def _host_call(sg, w, A_pin, B_pin, C_pin, stream):
+    """One C-ABI sgemm_host call: A, B and C in (pinned) host memory, copies inside."""
+    st = sg.load().sgemm_host(w.M, w.N, w.K, A_pin.data_ptr(), w.K, B_pin.data_ptr(), w.N,
+                              C_pin.data_ptr(), w.N, stream.cuda_stream)
+    if st != 0:
+        raise RuntimeError(f"sgemm_host failed: {sg.status_string(st)}")
+
+
+def e2e_pipelined(w, sg, device, A_h, B_h, steps, warmup, streams=3):
+    """Seconds for ``steps`` end-to-end steps, each one C-ABI ``sgemm_host`` call on pinned
+    host buffers (the library copies A and B in, multiplies and copies C out, overlapping
+    the copies with the multiply inside the call).  Calls go round-robin over ``streams``
+    streams, each with its own device staging, so one call's copies also overlap another
+    call's multiply."""
     import torch
     A_pin, B_pin = A_h.pin_memory(), B_h.pin_memory()
-    bufs = [(torch.empty_like(A_pin, device=device), torch.empty_like(B_pin, device=device),
-             torch.empty((w.M, w.N), device=device)) for _ in range(2)]
-    C_pin = [torch.empty((w.M, w.N), dtype=torch.float32).pin_memory() for _ in range(2)]
-    s_in, s_mm, s_out = (torch.cuda.Stream(device) for _ in range(3))
-    total = warmup + steps
-    ev = {k: [torch.cuda.Event() for _ in range(total)] for k in ("in", "mm", "out")}
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    C_pin = [torch.empty((w.M, w.N), dtype=torch.float32).pin_memory() for _ in range(streams)]
+    ss = [torch.cuda.Stream(device) for _ in range(streams)]
+    for i in range(max(warmup, streams)):       # every stream's staging allocated untimed
+        _host_call(sg, w, A_pin, B_pin, C_pin[i % streams], ss[i % streams])
     torch.cuda.synchronize(device)
-    for i in range(total):
-        if i == warmup:
-            s_in.wait_stream(s_out)
-            s_in.wait_stream(s_mm)
-            start.record(s_in)
-        A, B, C = bufs[i % 2]
-        with torch.cuda.stream(s_in):
-            if i >= 2:
-                s_in.wait_event(ev["mm"][i - 2])      # A, B of this buffer set are free
-            A.copy_(A_pin, non_blocking=True)
-            B.copy_(B_pin, non_blocking=True)
-            ev["in"][i].record(s_in)
-        s_mm.wait_event(ev["in"][i])
-        if i >= 2:
-            s_mm.wait_event(ev["out"][i - 2])         # C of this buffer set was read out
-        st = sg.sgemm_raw(w.M, w.N, w.K, A.data_ptr(), w.K, B.data_ptr(), w.N, C.data_ptr(), w.N,
-                          s_mm.cuda_stream, variant)
-        if st != 0:
-            raise RuntimeError(sg.status_string(st))
-        ev["mm"][i].record(s_mm)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(ev["mm"][i])
-            C_pin[i % 2].copy_(C, non_blocking=True)
-            ev["out"][i].record(s_out)
-    s_out.wait_stream(s_in)
-    s_out.wait_stream(s_mm)
-    end.record(s_out)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(ss[0])
+    for s in ss[1:]:
+        s.wait_event(start)
+    for i in range(steps):
+        _host_call(sg, w, A_pin, B_pin, C_pin[i % streams], ss[i % streams])
+    for s in ss[1:]:
+        ss[0].wait_stream(s)
+    end.record(ss[0])
     torch.cuda.synchronize(device)
     return start.elapsed_time(end) / 1e3
 
 
-def e2e_per_call(w, sg, device, variant, A_h, B_h, calls, warmup):
-    """Per-call latency (microseconds) of one unpipelined end-to-end call on one stream:
-    host-to-device copies of A and B from pinned memory, the C-ABI multiply, and the
-    device-to-host copy of C, bracketed by CUDA events on that stream."""
+def e2e_per_call(w, sg, device, A_h, B_h, calls, warmup):
+    """Per-call latency (microseconds) of one C-ABI ``sgemm_host`` call at a time on one
+    stream (pinned host A, B and C; the copies in and out happen inside the call),
+    bracketed by CUDA events on that stream."""
     import torch
     A_pin, B_pin = A_h.pin_memory(), B_h.pin_memory()
-    A = torch.empty_like(A_pin, device=device)
-    B = torch.empty_like(B_pin, device=device)
-    C = torch.empty((w.M, w.N), device=device)
     C_pin = torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()
     s = torch.cuda.Stream(device)
     times = []
     for i in range(warmup + calls):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(s):
-            e0.record(s)
-            A.copy_(A_pin, non_blocking=True)
-            B.copy_(B_pin, non_blocking=True)
-            st = sg.sgemm_raw(w.M, w.N, w.K, A.data_ptr(), w.K, B.data_ptr(), w.N, C.data_ptr(),
-                              w.N, s.cuda_stream, variant)
-            if st != 0:
-                raise RuntimeError(sg.status_string(st))
-            C_pin.copy_(C, non_blocking=True)
-            e1.record(s)
+        e0.record(s)
+        _host_call(sg, w, A_pin, B_pin, C_pin, s)
+        e1.record(s)
         s.synchronize()
         if i >= warmup:
             times.append(e0.elapsed_time(e1) * 1e3)
@@ -590,15 +571,17 @@ def run_ours(args):
     peak_run = ffma_peak_tflops(sms, clock["sm_mhz"]) if clock["sm_mhz"] else None
     traffic = measured_traffic(w.name)
 
-    # End to end through the C ABI with pinned host buffers: every step copies its
-    # inputs in, multiplies and copies C out.  Copies run on their own streams so
-    # that step i's copies overlap the multiply of step i-1 (two buffer sets).
+    # End to end through the C-ABI call with host buffers (sgemm_host): every step
+    # copies its inputs in, multiplies and copies C out, inside the call.  Steps go
+    # round-robin over three streams, so one step's copies also overlap another's
+    # multiply.
     e2e_steps = max(3, min(args.steps, 40))
-    e2e_total = e2e_pipelined(w, sg, device, variant, A_h, B_h, e2e_steps, warmup=3)
+    e2e_total = e2e_pipelined(w, sg, device, A_h, B_h, e2e_steps, warmup=3)
     e2e_total = max_over_ranks(e2e_total, world, device)
     e2e_value = aggregate(w.flops * e2e_steps, e2e_total, world)
-    # The same call unpipelined: copy in, multiply, copy out, one call at a time.
-    lat = e2e_per_call(w, sg, device, variant, A_h, B_h, calls=max(3, min(args.steps, 20)), warmup=2)
+    # The same call one at a time on one stream (its own copies still overlap its
+    # multiply, panel by panel).
+    lat = e2e_per_call(w, sg, device, A_h, B_h, calls=max(3, min(args.steps, 20)), warmup=2)
     lat_us = max_over_ranks(statistics.median(lat), world, device)
 
     # Secondary size (n = 1024) on the same device.
@@ -645,10 +628,12 @@ def run_ours(args):
                       "us_median": statistics.median(times2) * 1e3, "generic": generic2},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 4 * (w.M * w.K + w.K * w.N),
                 "d2h_bytes_per_step": 4 * w.M * w.N,
-                "pipelining": "copies of step i overlap the multiply of step i-1 (3 streams)",
+                "api": "sgemm_host (C ABI, pinned host A, B, C; copies inside the call)",
+                "pipelining": "row panels inside each call; calls round-robin over 3 streams",
                 "per_call": {"us_median": lat_us, "value": w.flops / (lat_us * 1e-6) / 1e12,
                              "unit": UNIT, "calls": len(lat),
-                             "what": "one stream, no overlap: H2D of A and B, sgemm, D2H of C"}},
+                             "what": "one sgemm_host call at a time on one stream: H2D of B, "
+                                     "then A and the multiply and the D2H of C in row panels"}},
         "context": context,
         "tf32_mode": tf32,
         "gpu_launches": args.steps,

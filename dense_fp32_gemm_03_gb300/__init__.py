@@ -6,11 +6,11 @@ synthetic workloads (``workloads``).
 """
 from .binding import (AUTO, GUARDED, SMALL, SPECIALIZED, STAGED, STREAMK, STREAMK_SMALL, TILED, TILED_SMALL, VARIANTS,
                       SgemmError, debug_expire_wait, debug_owner_publishes, load, query_device_status,
-                      release_workspaces, select_variant, sgemm, sgemm_ex, sgemm_ex2, sgemm_raw, sgemm_tf32, status_string,
+                      release_workspaces, select_variant, sgemm, sgemm_ex, sgemm_ex2, sgemm_host, sgemm_raw, sgemm_tf32, status_string,
                       ROW_MAJOR, COL_MAJOR, OP_N, OP_T,
                       variant_name, workspace_size)
 
-__all__ = ["sgemm", "sgemm_ex", "sgemm_ex2", "ROW_MAJOR", "COL_MAJOR", "OP_N", "OP_T", "sgemm_tf32", "sgemm_raw", "select_variant", "workspace_size", "query_device_status",
+__all__ = ["sgemm", "sgemm_ex", "sgemm_ex2", "sgemm_host", "ROW_MAJOR", "COL_MAJOR", "OP_N", "OP_T", "sgemm_tf32", "sgemm_raw", "select_variant", "workspace_size", "query_device_status",
            "debug_expire_wait", "debug_owner_publishes", "release_workspaces", "status_string", "variant_name", "load",
            "SgemmError", "VARIANTS", "AUTO", "GUARDED", "TILED", "STREAMK", "TILED_SMALL",
            "STREAMK_SMALL", "STAGED", "SPECIALIZED", "SMALL"]

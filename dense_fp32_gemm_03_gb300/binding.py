@@ -26,7 +26,7 @@ EXPORTS = ("sgemm", "sgemm_variant", "sgemm_select_variant", "sgemm_workspace_si
            "sgemm_query_device_status", "sgemm_release_workspaces", "sgemm_status_string",
            "sgemm_variant_name", "sgemm_debug_expire_wait", "sgemm_debug_owner_publishes",
            "sgemm_streamk_static",
-           "sgemm_tf32", "sgemm_ex", "sgemm_ex2")
+           "sgemm_tf32", "sgemm_ex", "sgemm_ex2", "sgemm_host")
 
 
 class SgemmError(RuntimeError):
@@ -88,6 +88,8 @@ def load(path: str | None = None):
         lib.sgemm_ex2.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, i64, i64, f32, vp,
                                   i64, vp, i64, f32, vp, i64, vp]
         lib.sgemm_ex2.restype = st
+        lib.sgemm_host.argtypes = gemm_args
+        lib.sgemm_host.restype = st
         _lib = lib
         return lib
 
@@ -227,6 +229,45 @@ def sgemm_ex2(A, B, C, alpha=1.0, beta=0.0, trans_a=False, trans_b=False, layout
     if st != OK:
         raise SgemmError(st, "sgemm_ex2")
     return C
+
+
+def sgemm_host(A, B, out=None, stream=None, wait: bool = True):
+    """C = A @ B for 2-D float32 CPU tensors, computed on the current CUDA device.
+
+    The library copies A and B to the device, multiplies and copies C back
+    (``sgemm_host`` in include/sgemm.h), on ``stream`` (default: the current
+    stream of the current device).  Pinned tensors (``pin_memory()``) give
+    asynchronous, overlapped copies.  ``out`` (M x N float32 CPU tensor, unit
+    column stride) receives C; by default a pinned tensor is allocated.  With
+    ``wait`` the call returns after the stream has finished; without it C is
+    complete only once the stream has.
+    """
+    import torch
+
+    def ld(t, name):
+        if t.device.type != "cpu" or t.dtype != torch.float32 or t.dim() != 2:
+            raise ValueError(f"{name} must be a 2-D float32 CPU tensor")
+        if t.shape[1] > 1 and t.stride(1) != 1:
+            raise ValueError(f"{name} must have unit column stride")
+        return max(t.stride(0), t.shape[1], 1)
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError(f"shapes do not match: A {tuple(A.shape)}, B {tuple(B.shape)}")
+    lda, ldb = ld(A, "A"), ld(B, "B")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, pin_memory=True)
+    if tuple(out.shape) != (M, N):
+        raise ValueError(f"out must be {M} x {N}")
+    ldc = ld(out, "out")
+    device = torch.cuda.current_device()
+    handle = _stream_handle(device, stream)
+    st = load().sgemm_host(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc, handle)
+    if st != OK:
+        raise SgemmError(st, "sgemm_host")
+    if wait:
+        (stream if stream is not None else torch.cuda.current_stream(device)).synchronize()
+    return out
 
 
 def sgemm_tf32(A, B, out=None, stream=None):

@@ -926,6 +926,7 @@ void sgemm_release_workspaces(void) {
   g_workspaces.clear();
   g_retired.clear();
   cudaSetDevice(cur);
+  gb300::host_staging_release();
 }
 
 const char* sgemm_status_string(sgemm_status_t s) {

@@ -108,4 +108,7 @@ cudaError_t launch_expire_probe(uint32_t* status, uint64_t limit_ns, cudaStream_
 // status[2..3] = status[0..1], then status[0..1] = 0 (status has four words).
 cudaError_t launch_status_take(uint32_t* status, cudaStream_t stream);
 
+// Frees sgemm_host()'s device staging, copy streams and events (every device).
+void host_staging_release();
+
 }  // namespace gb300

@@ -11,7 +11,8 @@
  * storage follows the same page's "Kernel 1" section; element (r, c) of a
  * matrix with row stride ld sits at base[r * ld + c].
  *
- * Memory and ownership.  A, B and C are DEVICE pointers owned by the caller;
+ * Memory and ownership.  A, B and C are DEVICE pointers owned by the caller
+ * (except for sgemm_host(), which takes host memory and copies it itself);
  * the library never frees or retains them past the call.  C must not overlap
  * A or B.  C is write-only: its previous contents (NaN included) are never
  * read.  All calls are asynchronous on `stream` (0 = legacy default stream):
@@ -151,6 +152,45 @@ typedef enum {
 sgemm_status_t sgemm_ex2(int layout, int trans_a, int trans_b, int64_t M, int64_t N, int64_t K,
                          float alpha, const float *A, int64_t lda, const float *B, int64_t ldb,
                          float beta, float *C, int64_t ldc, cudaStream_t stream);
+
+/*
+ * C = A * B as sgemm(), with A, B and C in HOST memory: the copies to the
+ * current device and back happen inside the call.  The product is the one
+ * of "Beyond Kernel 7: Closing the Gap to cuBLAS on an H100 FP32 GEMM",
+ * "The operation"; results are within the same bound as sgemm()'s (rows of C
+ * are computed by separate launches, so bits may differ from one sgemm() call
+ * over the whole product).
+ *
+ * Layout: row-major, element row strides lda >= K, ldb >= N, ldc >= N (any
+ * alignment).  The library copies B whole, then A in row panels (one panel
+ * below M = 2048, else M / 6 rows but at least 512) on a copy stream of its
+ * own.  It multiplies each panel on `stream` as soon as its rows have landed,
+ * and copies that panel's rows of C back on a second copy stream while the
+ * next panel is multiplied.
+ *
+ * Ownership and ordering: asynchronous on `stream` like cudaMemcpyAsync.
+ * The call returns once everything is enqueued, and C holds the product
+ * when `stream` has completed; A, B and C must stay valid and unmodified
+ * (C unread) until then.  Nothing of the call starts before work queued
+ * earlier on `stream` has completed.  Page-locked host memory
+ * (cudaHostAlloc, cudaHostRegister) gives asynchronous, overlapped copies.
+ * Pageable memory works too, but CUDA may then make the copies synchronous.
+ * C must not overlap A or B.
+ *
+ * Scratch: device staging of (M*K4 + K*N4 + M*N4) floats, K4 and N4 being K
+ * and N rounded up to multiples of 4, plus the Stream-K workspace of the
+ * panels.  Both come from caches the library keeps per (device, stream),
+ * grown with cudaMalloc the first time a call needs more, and freed by
+ * sgemm_release_workspaces().  The copy streams and events are created once
+ * per (device, stream).  Calls on one stream run one after another; calls on
+ * different streams have separate staging and may overlap.
+ *
+ * Errors: as sgemm() (SGEMM_ERR_ALLOC when the staging cannot be allocated);
+ * M == 0 or N == 0 is a no-op, K == 0 writes zeros to C.  After an error
+ * return, C's contents are undefined.
+ */
+sgemm_status_t sgemm_host(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                          const float *B, int64_t ldb, float *C, int64_t ldc, cudaStream_t stream);
 
 /*
  * As sgemm() but forces `variant` (an sgemm_variant_t).  The four pipelined

@@ -129,7 +129,38 @@ def test_ex2_checks_stored_leading_dimensions(lib, args):
     ta, tb, M, N, K, lda, ldb, ldc = args
     assert lib.sgemm_ex2(0, ta, tb, M, N, K, 1.0, P_A, lda, P_B, ldb, 0.0, P_C, ldc, None) == \
         binding.ERR_INVALID_VALUE
-    # The same leading dimensions are fine once they cover the stored rows.
+    # The same leading dimensions are fine once they cover the stored rows.  (Only
+    # without a GPU: with one, the fake addresses would reach a kernel.)
+    import torch
+    if torch.cuda.is_available():
+        return
     st = lib.sgemm_ex2(0, ta, tb, M, N, K, 1.0, P_A, max(lda, M if ta else K), P_B,
                        max(ldb, K if tb else N), 0.0, P_C, ldc, None)
     assert st != binding.ERR_INVALID_VALUE   # no device here: UNSUPPORTED
+
+
+# sgemm_host takes host addresses; its checks also run before any memory is touched.
+@pytest.mark.parametrize("args", [
+    (-1, 4, 4, P_A, 4, P_B, 4, P_C, 4),      # negative M
+    (4, 4, -1, P_A, 4, P_B, 4, P_C, 4),      # negative K
+    (4, 4, 8, P_A, 7, P_B, 4, P_C, 4),       # lda < K
+    (4, 8, 4, P_A, 4, P_B, 7, P_C, 8),       # ldb < N
+    (4, 8, 4, P_A, 4, P_B, 8, P_C, 7),       # ldc < N
+    (4, 4, 4, 0, 4, P_B, 4, P_C, 4),         # null A
+    (4, 4, 4, P_A, 4, P_B, 4, 0, 4),         # null C
+    (4, 4, 4, P_A, 4, P_B, 4, P_A + 16, 4),  # C overlaps A
+    (4, 4, 4, P_A, 4, P_B, 4, P_B + 60, 4),  # C overlaps B's last element
+])
+def test_host_entry_rejects_invalid_arguments(lib, args):
+    assert lib.sgemm_host(*args, None) == binding.ERR_INVALID_VALUE
+
+
+def test_host_entry_empty_and_oversized(lib):
+    assert lib.sgemm_host(0, 4, 4, 0, 4, 0, 4, 0, 4, None) == binding.OK    # M == 0: no-op
+    assert lib.sgemm_host(4, 0, 4, 0, 4, 0, 4, 0, 4, None) == binding.OK    # N == 0: no-op
+    assert lib.sgemm_host(2 ** 31, 4, 4, P_A, 4, P_B, 4, P_C, 4, None) == binding.ERR_UNSUPPORTED
+    # Valid arguments reach the device query: without a GPU, UNSUPPORTED.  (With a
+    # GPU the fake addresses would be copied from, so the call is not made there.)
+    import torch
+    if not torch.cuda.is_available():
+        assert lib.sgemm_host(4, 4, 4, P_A, 4, P_B, 4, P_C, 4, None) == binding.ERR_UNSUPPORTED
