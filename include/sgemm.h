@@ -183,7 +183,9 @@ sgemm_status_t sgemm_ex2(int layout, int trans_a, int trans_b, int64_t M, int64_
  * grown with cudaMalloc the first time a call needs more, and freed by
  * sgemm_release_workspaces().  The copy streams and events are created once
  * per (device, stream).  Calls on one stream run one after another; calls on
- * different streams have separate staging and may overlap.
+ * different streams have separate staging and may overlap.  As for sgemm(),
+ * calls on one stream must not be made from several host threads at the same
+ * time (they share that stream's staging and events).
  *
  * Errors: as sgemm() (SGEMM_ERR_ALLOC when the staging cannot be allocated);
  * M == 0 or N == 0 is a no-op, K == 0 writes zeros to C.  After an error
