@@ -64,17 +64,32 @@ int64_t panel_rows(int64_t M) {
   return round_up(rows, kPanelAlign);
 }
 
+void destroy_sync_objects(HostStaging& s) {
+  for (int p = 0; p < kMaxPanels; ++p) {
+    if (s.landed[p]) cudaEventDestroy(s.landed[p]);
+    if (s.multiplied[p]) cudaEventDestroy(s.multiplied[p]);
+    s.landed[p] = s.multiplied[p] = nullptr;
+  }
+  if (s.start) cudaEventDestroy(s.start);
+  if (s.done) cudaEventDestroy(s.done);
+  if (s.in) cudaStreamDestroy(s.in);
+  if (s.out) cudaStreamDestroy(s.out);
+  s.start = s.done = nullptr;
+  s.in = s.out = nullptr;
+}
+
+// All or nothing: after a failure nothing is left half-made, and the next
+// call tries again.
 bool create_sync_objects(HostStaging& s) {
-  if (cudaStreamCreateWithFlags(&s.in, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaStreamCreateWithFlags(&s.out, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaEventCreateWithFlags(&s.start, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming) != cudaSuccess)
-    return false;
-  for (int p = 0; p < kMaxPanels; ++p)
-    if (cudaEventCreateWithFlags(&s.landed[p], cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&s.multiplied[p], cudaEventDisableTiming) != cudaSuccess)
-      return false;
-  return true;
+  bool ok = cudaStreamCreateWithFlags(&s.in, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&s.out, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&s.start, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming) == cudaSuccess;
+  for (int p = 0; ok && p < kMaxPanels; ++p)
+    ok = cudaEventCreateWithFlags(&s.landed[p], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&s.multiplied[p], cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) destroy_sync_objects(s);
+  return ok;
 }
 
 // The staging of (dev, stream), holding at least `bytes`; nullptr on failure.
@@ -129,14 +144,7 @@ void host_staging_release() {
     cudaSetDevice(kv.first.first);
     cudaDeviceSynchronize();
     if (s.buf) cudaFree(s.buf);
-    for (int p = 0; p < kMaxPanels; ++p) {
-      if (s.landed[p]) cudaEventDestroy(s.landed[p]);
-      if (s.multiplied[p]) cudaEventDestroy(s.multiplied[p]);
-    }
-    if (s.start) cudaEventDestroy(s.start);
-    if (s.done) cudaEventDestroy(s.done);
-    if (s.in) cudaStreamDestroy(s.in);
-    if (s.out) cudaStreamDestroy(s.out);
+    destroy_sync_objects(s);
   }
   for (auto& r : g_retired) {
     cudaSetDevice(r.first);
