@@ -196,12 +196,17 @@ __global__ void __launch_bounds__(kSmThreads)
   float4* slots = reinterpret_cast<float4*>(p.partials) + int64_t(tile) * p.splits * kSlotVec;
 #pragma unroll
   for (int j = 0; j < kSmVec; ++j) __stcg(slots + share * kSlotVec + j * kSmThreads + tid, value(j));
-  __threadfence();
+  // One thread releases the partial: the barrier orders every thread's stores
+  // before its GPU-scope fence (cumulative), the fence before the arrival, and
+  // a second fence orders the last arriver's reads below.
   __syncthreads();
-  if (tid == 0) sm.last = atomicAdd(p.counters + tile, 1) == p.splits - 1 ? 1 : 0;
+  if (tid == 0) {
+    __threadfence();
+    sm.last = atomicAdd(p.counters + tile, 1) == p.splits - 1 ? 1 : 0;
+    __threadfence();
+  }
   __syncthreads();
   if (!sm.last) return;
-  __threadfence();
   float4 sum[kSmVec];
 #pragma unroll 1
   for (int sh = 0; sh < p.splits; ++sh) {
