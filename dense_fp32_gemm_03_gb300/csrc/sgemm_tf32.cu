@@ -448,15 +448,19 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                      make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
                                  __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
           }
-          __threadfence();
+          // One thread releases the partial (cumulative fence after the
+          // barrier); its second fence orders a last arriver's reads.
           dev::named_barrier(1, kTfEpiThreads);
-          if (etid == 0) *s_last = atomicAdd(args.counters + u.t_sk, 1) == others ? 1 : 0;
+          if (etid == 0) {
+            __threadfence();
+            *s_last = atomicAdd(args.counters + u.t_sk, 1) == others ? 1 : 0;
+            __threadfence();
+          }
           dev::named_barrier(1, kTfEpiThreads);
           last = *s_last != 0;
           dev::named_barrier(1, kTfEpiThreads);  // s_last may be rewritten by the next split tile
         }
         if (last) {
-          __threadfence();
           const float4* base = reinterpret_cast<const float4*>(args.partials) + row_local;
           // 64 columns per step: every slot's 16 loads of a step are in flight together.
 #pragma unroll 1
@@ -818,15 +822,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTfThreads, 1)
                      make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
                                  __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
           }
-          __threadfence();
+          // One thread releases the partial (cumulative fence after the
+          // barrier); its second fence orders a last arriver's reads.
           dev::named_barrier(1, kTfEpiThreads);
-          if (etid == 0) *s_last = atomicAdd(counter, 1) == others ? 1 : 0;
+          if (etid == 0) {
+            __threadfence();
+            *s_last = atomicAdd(counter, 1) == others ? 1 : 0;
+            __threadfence();
+          }
           dev::named_barrier(1, kTfEpiThreads);
           last = *s_last != 0;
           dev::named_barrier(1, kTfEpiThreads);
         }
         if (last) {
-          __threadfence();
           const float4* base = reinterpret_cast<const float4*>(args.partials) + row_local;
 #pragma unroll 1
           for (int c = 0; c < kPrBN; c += 64) {
