@@ -9,7 +9,6 @@ views, pageable memory, K == 0, two streams at once and staging regrowth.
 """
 import os
 
-import numpy as np
 import pytest
 import torch
 
