@@ -51,7 +51,9 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="square_4096_uniform")
-    p.add_argument("--variant", default="auto")
+    p.add_argument("--variant", default="auto",
+                   help="kernel variant of the timed device steps (the end-to-end figure goes "
+                        "through sgemm_host, which always lets the selector choose)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target host time of the oracle sample")
