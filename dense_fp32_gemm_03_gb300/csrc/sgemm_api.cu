@@ -876,6 +876,7 @@ sgemm_status_t sgemm_tf32(int64_t M, int64_t N, int64_t K, const float* A, int64
   args.status = ds->status;
   args.wait_limit_ns = kDefaultWaitLimitNs;
   args.c_scalar = c_scalar ? 1 : 0;
+  args.owner_publishes = g_owner_publishes.load(std::memory_order_relaxed);
   const cudaError_t e =
       pair ? gb300::launch_tf32_pair_kernel(b_mn, tmap_a, tmap_b, tmap_c, args, lp.sc, int(lp.grid),
                                              stream)

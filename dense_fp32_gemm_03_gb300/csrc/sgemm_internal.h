@@ -32,6 +32,7 @@ struct Tf32Args {
   uint32_t* status;   // device status word
   uint64_t wait_limit_ns;
   int32_t c_scalar;   // C is not 16-byte aligned row by row: 4-byte stores
+  int32_t owner_publishes;  // test switch: as GemmArgs::owner_publishes (sgemm_plan.h)
 };
 // tmap_a: A (K fastest), box {32, 128}, 128-byte swizzle.  b_mn: tmap_b is B itself (N
 // fastest), box {32, 32}, 128-byte swizzle of 32-byte atoms; otherwise tmap_b is Bt (K

@@ -428,7 +428,7 @@ __global__ void __launch_bounds__(kTfThreads, 1)
         const int c_first = sk_owner(sc, t_first_iter);
         const int c_last = sk_owner(sc, t_first_iter + sc.iters_per_tile - 1);
         const int others = c_last - c_first;
-        const bool own_first = cta == c_first;
+        const bool own_first = cta == c_first && !args.owner_publishes;
         bool last = false;
         if (own_first) {
           if (etid == 0) *s_last = dev::ld_acquire_gpu(args.counters + u.t_sk) == others ? 1 : 0;
@@ -800,7 +800,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTfThreads, 1)
         const int c_first = sk_owner(sc, t_first_iter);
         const int c_last = sk_owner(sc, t_first_iter + sc.iters_per_tile - 1);
         const int others = c_last - c_first;
-        const bool own_first = pair == c_first;
+        const bool own_first = pair == c_first && !args.owner_publishes;
         int32_t* counter = args.counters + 2 * u.t_sk + int(rank);
         bool last = false;
         if (own_first) {

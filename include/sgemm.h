@@ -290,10 +290,10 @@ sgemm_status_t sgemm_debug_expire_wait(uint64_t limit_ns, cudaStream_t stream);
 /*
  * Test hook for the Stream-K fix-up ("Beyond Kernel 7: Closing the Gap to
  * cuBLAS on an H100 FP32 GEMM", section "Kernel 14").  When `on` is nonzero,
- * pipelined launches made after this call (by any thread of the process) have
- * the CTA that owns a split tile's first k-tiles publish its partial sum like
- * every other sharer.  It never keeps its partial in registers or prefetches
- * the others'.  The last CTA to arrive then sums every partial from the
+ * pipelined and TF32 launches made after this call (by any thread of the
+ * process) have the CTA (or CTA pair) that owns a split tile's first k-tiles
+ * publish its partial sum like every other sharer.  It never keeps its
+ * partial in registers or tensor memory, and never prefetches the others'.  The last CTA to arrive then sums every partial from the
  * workspace in CTA order.  The additions are the same sequence as on the
  * default path, so results must be bit-identical; only speed differs.  The
  * switch is process-wide; pass 0 to restore the default.  No error cases.

@@ -204,6 +204,25 @@ def test_tf32_stream_k_deterministic_and_within_bound(shape):
     check_tf32(C1[r.cuda(), c.cuda()].cpu().numpy(), ref, E, K, f"tf32 {shape}")
 
 
+@pytest.mark.parametrize("shape", [(2048, 2048, 2048), (1000, 1000, 2048), (4096, 4096, 512)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_tf32_split_tiles_summed_from_the_workspace_match_bit_for_bit(shape):
+    """With the test switch the owner of a split tile publishes its partial instead of
+    keeping it in tensor memory, and the last to arrive sums every partial from the
+    workspace: the same additions in the same order, so the same bits."""
+    M, N, K = shape
+    A = workloads.matrix(M, K, "uniform", 98, 0).cuda()
+    B = workloads.matrix(K, N, "uniform", 98, 1).cuda()
+    default = sg.sgemm_tf32(A, B)
+    sg.debug_owner_publishes(True)
+    try:
+        published = sg.sgemm_tf32(A, B)
+    finally:
+        sg.debug_owner_publishes(False)
+    torch.cuda.synchronize()
+    assert torch.equal(default, published)
+
+
 _SINGLE_SM_SCRIPT = r"""
 import sys, numpy as np, torch
 sys.path.insert(0, {root!r})
@@ -232,6 +251,16 @@ for (M, N, K) in [(200, 261, 64), (1029, 2051, 64), (2600, 2301, 256)]:
     torch.cuda.synchronize()
     assert np.array_equal(big[:M, :N].cpu().numpy().astype(np.float64), ref), (M, N, K)
     assert bool(torch.isnan(big[:M, N:]).all()) and bool(torch.isnan(big[M:]).all()), (M, N, K)
+# Split tiles summed from the workspace (test switch) give the owner's bits.
+for (M, N, K) in [(1000, 1000, 2048), (4096, 4096, 512)]:
+    A = workloads.matrix(M, K, "uniform", 99, 0).cuda()
+    B = workloads.matrix(K, N, "uniform", 99, 1).cuda()
+    C0 = sg.sgemm_tf32(A, B)
+    sg.debug_owner_publishes(True)
+    C1 = sg.sgemm_tf32(A, B)
+    sg.debug_owner_publishes(False)
+    torch.cuda.synchronize()
+    assert torch.equal(C0, C1), (M, N, K)
 assert sg.query_device_status() == (0, 0)
 print("single-SM path ok")
 """
