@@ -268,7 +268,8 @@ sgemm_status_t sgemm_query_device_status(cudaStream_t stream, uint32_t *detail);
 
 /*
  * Frees every cached workspace of every device, including those replaced by
- * larger ones (synchronises each device first).  CUDA graphs captured with
+ * larger ones, and sgemm_host()'s device staging, copy streams and events
+ * (synchronises each device first).  CUDA graphs captured with
  * sgemm() calls must not be replayed afterwards.
  */
 void sgemm_release_workspaces(void);
